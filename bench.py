@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the GDN state-scan hot path on GB300.
+
+One step = one pass of the whole path over one batch of the 8 x 16-head,
+N = 8192, bf16 prefill workload:
+  1. gdn_prefill_ckpt     : scan with bf16 readout and 16 equally spaced fp32
+                            checkpoints per sequence (index plan on the host);
+  2. gdn_resume_from_ckpt : 16 resume probes (sequence ~ U, depth ~ U[1, N])
+                            recomputing c_j+1..d with readout;
+  3. gdn_tail_replay      : Tail-Replay at m = N with r = 5 % (k = 410) from
+                            a zero state.
+value = whole-job tok*head per second over all ranks, device-timed with
+inputs resident in HBM; e2e = the same step through the Python/C API with
+pinned host inputs copied in and every result copied out each step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 run under torchrun: every rank scans its own batch (weak scaling,
+no collective on the data path; the barrier and a max-reduction of the
+elapsed time are the only cross-rank calls).
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "GDN scan Mtok·head/s (prefill+ckpt, resume, tail replay)"
+UNIT = "Mtok·head/s"
+WORKLOAD = "prefill"
+N_PROBES = 16
+REPLAY_R = (1, 20)
+FP32_LANES_PER_SM = 128
+SM_COUNT = 152
+SM_MAX_MHZ = 2070.0
+PEAK_ALU_TFLOPS = SM_COUNT * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12  # 80.54
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_scan_prefill_8x16x8192.md")
+KERNEL_SRC = os.path.join(ROOT, "hybrid_model_recurrent_gb300", "csrc", "gdn_kernel.cuh")
+
+
+# -------------------------------------------------------------------------------------------
+# distributed plumbing
+# -------------------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, elapsed_s: float, ws: int, device):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    total = sum_over_ranks(units_per_rank, ws, device)
+    slowest = max_over_ranks(elapsed_s, ws, device)
+    return total, slowest, total / slowest
+
+
+# -------------------------------------------------------------------------------------------
+# clocks during the timed region
+# -------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------------------------------------
+# the step
+# -------------------------------------------------------------------------------------------
+class Step:
+    def __init__(self, w: synth.Workload, device):
+        import hybrid_model_recurrent_gb300 as gdn
+        self.gdn = gdn
+        self.w = w
+        self.dev = device
+        self.cu = w.cu_seqlens
+        self.ck = w.ckpt_positions()
+        self.probes = dataclasses.replace(w, n_probes=N_PROBES).probes()
+        self.m = list(w.seq_lens)
+        T, H, dk, dv, B = w.T, w.H, w.dk, w.dv, w.B
+        f32 = torch.float32
+        self.inp = synth.make_inputs(w, device=device)
+        self.o = torch.empty((T, H, dv), dtype=w.out_dtype, device=device)
+        self.S_final = torch.empty((B, H, dv, dk), dtype=f32, device=device)
+        n_ck = sum(len(c) for c in self.ck)
+        self.ckpt = torch.empty((n_ck, H, dv, dk), dtype=f32, device=device)
+        self.chosen = []
+        rows = 0
+        for s, d in self.probes:
+            j = gdn.gdn_select_ckpt(self.ck[s], d)
+            rows += d - (0 if j < 0 else self.ck[s][j])
+        self.resume_rows = rows
+        self.o_res = torch.empty((max(rows, 1), H, dv), dtype=w.out_dtype, device=device)
+        self.S_out = torch.empty((len(self.probes), H, dv, dk), dtype=f32, device=device)
+        self.S_hat = torch.empty((B, H, dv, dk), dtype=f32, device=device)
+        self.replay_tokens = sum(gdn.gdn_replay_plan(m, *REPLAY_R)[1] for m in self.m)
+        self.tok_head = {"prefill": T * H, "resume": rows * H, "replay": self.replay_tokens * H}
+        self.ws = gdn.workspace(device)
+        self.launches_per_step = 3
+        self.ev = None
+
+    def units(self) -> int:
+        return sum(self.tok_head.values())
+
+    def run(self, inp=None, record=None):
+        g = self.gdn
+        inp = inp or self.inp
+        s = torch.cuda.current_stream(self.dev)
+        if record is not None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+        g.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, ckpt_pos=self.ck, o=self.o,
+                           S_final=self.S_final, ckpt_states=self.ckpt, ws=self.ws)
+        if record is not None:
+            e1.record(s)
+            record.append((e0, e1))
+        g.gdn_resume_from_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, self.ckpt, self.ck, self.probes,
+                               o_out=self.o_res, S_out=self.S_out, ws=self.ws)
+        g.gdn_tail_replay(None, inp.k, inp.v, inp.alpha, inp.beta, self.cu, self.m, *REPLAY_R, S_hat=self.S_hat,
+                          ws=self.ws)
+
+    def outputs(self):
+        return [self.o, self.S_final, self.ckpt, self.S_out, self.o_res[:self.resume_rows], self.S_hat]
+
+
+def profile_traffic():
+    """DRAM bytes per launch of the prefill kernel from the committed ncu summary,
+    only if it was taken on the current kernel source."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+        with open(KERNEL_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip().strip("`- ")] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# -------------------------------------------------------------------------------------------
+def oracle_jobs(w: synth.Workload, pairs, tokens: int):
+    """Oracle jobs for `pairs` (seq, head) streams of `tokens` tokens each: prefill
+    with readout and the workload's checkpoints (inputs generated here, untimed)."""
+    import oracle
+    oracle.build()
+    jobs = []
+    for b, h in pairs:
+        t0 = w.cu_seqlens[b]
+        inp = synth.make_inputs(w, t_range=(t0, t0 + tokens), heads=range(h, h + 1))
+        ck = [c for c in w.ckpt_positions()[b] if c <= tokens]
+        jobs.append(lambda i=inp, ck=ck: oracle.prefill(i.q[:, 0], i.k[:, 0], i.v[:, 0], i.alpha[:, 0],
+                                                        i.beta[:, 0], ckpt_pos=ck))
+    return jobs
+
+
+def time_oracle(jobs, threads: int) -> float:
+    import oracle
+    t = time.perf_counter()
+    oracle.run_many(jobs, threads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(w: synth.Workload):
+    threads = os.cpu_count() or 1
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H)][: 2 * threads]
+    dt = time_oracle(oracle_jobs(w, pairs, w.seq_lens[0]), threads)
+    units = len(pairs) * w.seq_lens[0]
+    return {"value": units / dt / 1e6, "unit": UNIT, "cores": min(threads, len(pairs)), "kind": "oracle",
+            "sample": f"fp64 oracle prefill (readout + 16 checkpoints) of {len(pairs)} of the "
+                      f"{w.B * w.H} (sequence, head) streams, {w.seq_lens[0]} tokens each "
+                      f"({units} tok*head, {dt:.1f} s on {min(threads, len(pairs))} threads)"}
+
+
+def config_dict(w, ws):
+    return {"workload": "prefill+ckpt 8x16 heads, N=8192, dk=dv=128, bf16 q/k/v/o, fp32 state, M=16 ckpts; "
+                        f"+{N_PROBES} resume probes; +tail replay r=5% at m=N",
+            "seqs_per_rank": w.B, "heads": w.H, "seq_len": w.seq_lens[0], "d_k": w.dk, "d_v": w.dv,
+            "ckpts_per_seq": len(w.ckpt_positions()[0]), "resume_probes": N_PROBES,
+            "replay_r": f"{REPLAY_R[0]}/{REPLAY_R[1]}", "parallelism": f"dp{ws} (weak: one batch per rank)",
+            "l2": "inputs larger than L2 (805 MB of bf16 q/k/v streamed per step)", "seed": 0}
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = synth.workload(WORKLOAD, seed=0)
+    threads = os.cpu_count() or 1
+    steps, warm = args.steps, args.warmup
+    budget_s = 150.0
+    rate = 256 / max(time_oracle(oracle_jobs(w, [(0, 0)], 256), 1), 1e-6)  # tok*head/s per thread
+    per_step_s = budget_s / max(steps + warm, 1)
+    tokens = int(max(32, min(w.seq_lens[0], rate * per_step_s)))
+    pairs = [(b % w.B, (b // w.B) % w.H) for b in range(threads)]
+    jobs = oracle_jobs(w, pairs, tokens)
+    for _ in range(warm):
+        time_oracle(jobs, threads)
+    dt = sum(time_oracle(jobs, threads) for _ in range(steps))
+    units = len(pairs) * tokens * steps
+    val = units / dt / 1e6
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+            "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "impl": "reference",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": config_dict(w, args.gpus),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"per step: fp64 oracle prefill (readout + checkpoints) of {len(pairs)} "
+                                       f"(sequence, head) streams x {tokens} tokens, one per host thread"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------------------------------
+# our arm
+# -------------------------------------------------------------------------------------------
+def run_ours(args, ws, rank, local):
+    import hybrid_model_recurrent_gb300 as gdn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    gdn.build()
+    w = synth.workload(WORKLOAD, seed=rank)
+    step = Step(w, dev)
+    gdn.clear_status(dev)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-timed region ----
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    rec = []
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record()
+    for _ in range(args.steps):
+        step.run(record=rec)
+    e_end.record()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    elapsed = e_start.elapsed_time(e_end) / 1e3
+    status = gdn.read_status(dev)
+    if status != gdn.GDN_OK:
+        raise RuntimeError(f"device status {gdn.status_string(status)} during the timed region")
+    units = step.units() * args.steps
+    total, slowest, thr = aggregate(units, elapsed, ws, dev)
+    prefill_ms = statistics.mean(a.elapsed_time(b) for a, b in rec)
+
+    # ---- end to end: pinned host inputs in, every result out, each step ----
+    host_in = [t.cpu().pin_memory() for t in (step.inp.q, step.inp.k, step.inp.v, step.inp.alpha, step.inp.beta)]
+    dev_in = synth.Inputs(*[torch.empty_like(t) for t in (step.inp.q, step.inp.k, step.inp.v, step.inp.alpha,
+                                                           step.inp.beta)])
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.outputs()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(3, min(args.steps, 30))
+
+    def e2e_step():
+        for d_, h_ in zip((dev_in.q, dev_in.k, dev_in.v, dev_in.alpha, dev_in.beta), host_in):
+            d_.copy_(h_, non_blocking=True)
+        step.run(inp=dev_in)
+        for h_, d_ in zip(host_out, step.outputs()):
+            h_.copy_(d_, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_step()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_el = time.perf_counter() - t0
+    barrier(ws)
+    _, _, e2e_thr = aggregate(step.units() * e2e_steps, e2e_el, ws, dev)
+
+    flops_per_launch = 3 * w.dv * w.dk * 2 * w.T * w.H   # 3 FMAs per state element per tok*head
+    achieved = flops_per_launch / (prefill_ms * 1e-3) / 1e12
+    base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": thr / 1e6, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": slowest / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 q/k/v/o)",
+            "data": "synthetic (seeded counter-based generator)", "config": config_dict(w, ws),
+            "e2e": {"value": e2e_thr / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": step.launches_per_step * args.steps,
+            "roofline": {"bound": "alu", "kernel": "gdn_scan_kernel<128,bf16,bf16,readout> (prefill)",
+                         "achieved": achieved, "peak": PEAK_ALU_TFLOPS, "unit": "TFLOP/s",
+                         "frac": achieved / PEAK_ALU_TFLOPS, "traffic": profile_traffic(),
+                         "launch_ms": prefill_ms, "algorithmic_flops_per_launch": flops_per_launch,
+                         "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz (derived, not measured)"},
+            "phases": {k: v for k, v in step.tok_head.items()},
+            "states_per_s": sum(len(c) for c in step.ck) * w.H * args.steps / slowest,
+            "cpu_baseline": base,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

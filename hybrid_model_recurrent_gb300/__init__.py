@@ -1,0 +1,300 @@
+"""Python binding of the GB300 Gated DeltaNet state-scan library (libgdn_scan.so).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels.  Torch tensors are used for device memory and streams; outputs that
+the caller does not pass are allocated here.  The names follow the C ABI in
+``include/gdn_scan.h``:
+
+* ``gdn_prefill_ckpt``      prefill with exact state dumps at sparse positions
+* ``gdn_resume_from_ckpt``  resume at overlap depth d from the deepest stored state
+* ``gdn_tail_replay``       Tail-Replay from a zero state at a = m - ceil(r m)
+* host helpers ``gdn_replay_plan``, ``gdn_select_ckpt``, status utilities.
+
+There is no fallback: if the compiled library is missing the import of a
+compute entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn_scan.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = range(5)
+GDN_F32, GDN_BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+_workspaces: Dict[int, torch.Tensor] = {}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("cu_seqlens", ctypes.POINTER(ctypes.c_int64)),
+                ("qkv_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with hybrid_model_recurrent_gb300.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            P = ctypes.POINTER(_Problem)
+            pi64 = ctypes.POINTER(ctypes.c_int64)
+            pi32 = ctypes.POINTER(ctypes.c_int32)
+            L.gdn_prefill_ckpt.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, pi64, pi64, vp, vp, sz, vp]
+            L.gdn_resume_from_ckpt.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, pi64, pi64, i32, pi32, pi64, vp, vp,
+                                               pi64, pi64, vp, sz, vp]
+            L.gdn_tail_replay.argtypes = [P, vp, vp, vp, vp, vp, pi64, i32, i32, vp, vp, vp, vp, pi64, pi64, vp, sz,
+                                          vp]
+            L.gdn_replay_plan.argtypes = [i64, i32, i32, pi64, pi64]
+            L.gdn_select_ckpt.argtypes = [pi64, i32, i64, pi32]
+            L.gdn_workspace_size.argtypes = []
+            L.gdn_workspace_size.restype = sz
+            L.gdn_clear_status.argtypes = [vp, sz, vp]
+            L.gdn_read_status.argtypes = [vp, sz, vp]
+            L.gdn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.gdn_set_wait_limit_ns.restype = None
+            L.gdn_status_string.argtypes = [ctypes.c_int]
+            L.gdn_status_string.restype = ctypes.c_char_p
+            for f in ("gdn_prefill_ckpt", "gdn_resume_from_ckpt", "gdn_tail_replay", "gdn_replay_plan",
+                      "gdn_select_ckpt", "gdn_clear_status", "gdn_read_status"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().gdn_status_string(int(s)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != GDN_OK:
+        raise GdnError(rc, where)
+
+
+def _i64(values) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(list(values), dtype=np.int64))
+
+
+def _p64(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return GDN_F32
+    if dt == torch.bfloat16:
+        return GDN_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def workspace(device) -> torch.Tensor:
+    """The cached per-device workspace (holds the sticky device status word)."""
+    device = torch.device(device)
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(idx)
+    if ws is None:
+        ws = torch.zeros(int(lib().gdn_workspace_size()), dtype=torch.uint8, device=torch.device("cuda", idx))
+        _workspaces[idx] = ws
+    return ws
+
+
+def read_status(device=None, stream=None, ws: Optional[torch.Tensor] = None) -> int:
+    device = torch.device(device or "cuda")
+    ws = ws if ws is not None else workspace(device)
+    return lib().gdn_read_status(_ptr(ws), ws.numel(), _stream(stream, ws.device))
+
+
+def clear_status(device=None, stream=None, ws: Optional[torch.Tensor] = None) -> None:
+    device = torch.device(device or "cuda")
+    ws = ws if ws is not None else workspace(device)
+    _check(lib().gdn_clear_status(_ptr(ws), ws.numel(), _stream(stream, ws.device)), "gdn_clear_status")
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().gdn_set_wait_limit_ns(int(ns))
+
+
+def gdn_replay_plan(m: int, r_num: int, r_den: int):
+    """(a, k) with k = ceil(r_num * m / r_den) computed exactly, a = m - k."""
+    a, k = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().gdn_replay_plan(m, r_num, r_den, ctypes.byref(a), ctypes.byref(k)), "gdn_replay_plan")
+    return a.value, k.value
+
+
+def gdn_select_ckpt(c: Sequence[int], d: int) -> int:
+    """0-based index of the deepest c_i <= d, or -1."""
+    arr = _i64(c)
+    j = ctypes.c_int32()
+    _check(lib().gdn_select_ckpt(_p64(arr) if len(arr) else None, len(arr), d, ctypes.byref(j)),
+           "gdn_select_ckpt")
+    return j.value
+
+
+def _problem(cu: np.ndarray, H: int, dk: int, dv: int, qkv_dtype: torch.dtype, out_dtype: torch.dtype):
+    pr = _Problem()
+    pr.num_seqs = len(cu) - 1
+    pr.num_heads = H
+    pr.d_k = dk
+    pr.d_v = dv
+    pr.cu_seqlens = _p64(cu)
+    pr.qkv_dtype = _dtype_code(qkv_dtype)
+    pr.out_dtype = _dtype_code(out_dtype)
+    return pr
+
+
+def _flatten_ckpts(ckpt_pos, B: int):
+    """Per-sequence position lists -> (concatenated int64, cu_ckpt int64)."""
+    if ckpt_pos is None:
+        return None, None
+    cu = [0]
+    flat: List[int] = []
+    for lst in ckpt_pos:
+        flat.extend(int(x) for x in lst)
+        cu.append(len(flat))
+    if len(cu) != B + 1:
+        raise ValueError("ckpt_pos must give one list per sequence")
+    return _i64(flat), _i64(cu)
+
+
+def gdn_prefill_ckpt(q, k, v, alpha, beta, cu_seqlens, *, S0=None, ckpt_pos=None, readout: bool = True,
+                     out_dtype: Optional[torch.dtype] = None, o=None, S_final=None, ckpt_states=None,
+                     stream=None, ws: Optional[torch.Tensor] = None):
+    """Prefill with sparse checkpoints.  ckpt_pos: one list of 1-based positions per sequence.
+
+    Returns dict(o=[T,H,dv] or None, S_final=[B,H,dv,dk], ckpt_states=[M_total,H,dv,dk])."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    out_dtype = out_dtype or k.dtype
+    if readout and o is None:
+        o = torch.empty((T, H, dv), dtype=out_dtype, device=dev)
+    if not readout:
+        o = None
+    if S_final is None:
+        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    flat, cu_ck = _flatten_ckpts(ckpt_pos, B)
+    n_ck = 0 if cu_ck is None else int(cu_ck[-1])
+    if ckpt_states is None and n_ck > 0:
+        ckpt_states = torch.empty((n_ck, H, dv, dk), dtype=torch.float32, device=dev)
+    ws = ws if ws is not None else workspace(dev)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype)
+    rc = lib().gdn_prefill_ckpt(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
+                                _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
+                                _p64(flat) if n_ck > 0 else None, _p64(cu_ck), _ptr(ckpt_states),
+                                _ptr(ws), ws.numel(), _stream(stream, dev))
+    _check(rc, "gdn_prefill_ckpt")
+    return {"o": o, "S_final": S_final, "ckpt_states": ckpt_states}
+
+
+def gdn_resume_from_ckpt(q, k, v, alpha, beta, cu_seqlens, ckpt_states, ckpt_pos, probes, *, S0=None,
+                         readout: bool = True, out_dtype: Optional[torch.dtype] = None, S_out=None, o_out=None,
+                         stream=None, ws: Optional[torch.Tensor] = None):
+    """Resume at the probes' depths.  probes: list of (seq, depth).
+
+    Returns dict(S_out=[P,H,dv,dk], o=[R,H,dv] or None, chosen=[P] positions c_j, offsets=[P+1])."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    out_dtype = out_dtype or k.dtype
+    flat, cu_ck = _flatten_ckpts(ckpt_pos, B)
+    n_ck = 0 if cu_ck is None else int(cu_ck[-1])
+    P = len(probes)
+    seqs = np.ascontiguousarray(np.asarray([int(s) for s, _ in probes], dtype=np.int32))
+    deps = _i64(int(d) for _, d in probes)
+    chosen = np.zeros(P, dtype=np.int64)
+    offs = np.zeros(P + 1, dtype=np.int64)
+    # first pass: host plan (no launch) to size the packed readout
+    if readout and o_out is None:
+        rows = 0
+        for s, d in probes:
+            lst = list(ckpt_pos[s]) if ckpt_pos is not None else []
+            j = gdn_select_ckpt(lst, int(d))
+            rows += int(d) - (0 if j < 0 else lst[j])
+        o_out = torch.empty((max(rows, 0), H, dv), dtype=out_dtype, device=dev)
+    if not readout:
+        o_out = None
+    if S_out is None:
+        S_out = torch.empty((P, H, dv, dk), dtype=torch.float32, device=dev)
+    ws = ws if ws is not None else workspace(dev)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype)
+    rc = lib().gdn_resume_from_ckpt(
+        ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
+        _ptr(ckpt_states), _p64(flat) if n_ck > 0 else None, _p64(cu_ck), P,
+        seqs.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if P else None, _p64(deps) if P else None,
+        _ptr(S_out), _ptr(o_out), _p64(chosen) if P else None, _p64(offs), _ptr(ws), ws.numel(),
+        _stream(stream, dev))
+    _check(rc, "gdn_resume_from_ckpt")
+    return {"S_out": S_out, "o": o_out, "chosen": chosen.tolist(), "offsets": offs.tolist()}
+
+
+def gdn_tail_replay(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int, *, S_a=None, readout: bool = False,
+                    out_dtype: Optional[torch.dtype] = None, S_hat=None, S_exact=None, o=None, stream=None,
+                    ws: Optional[torch.Tensor] = None):
+    """Tail-Replay at matched lengths m (one per sequence).
+
+    Returns dict(S_hat, S_exact or None, o or None, a=[B], k=[B])."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    out_dtype = out_dtype or k.dtype
+    mm = _i64(m)
+    if S_hat is None:
+        S_hat = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    if S_a is not None and S_exact is None:
+        S_exact = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    if readout and o is None:
+        o = torch.zeros((T, H, dv), dtype=out_dtype, device=dev)
+    if not readout:
+        o = None
+    a_out = np.zeros(B, dtype=np.int64)
+    k_out = np.zeros(B, dtype=np.int64)
+    ws = ws if ws is not None else workspace(dev)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype)
+    rc = lib().gdn_tail_replay(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
+                               _ptr(beta), _p64(mm), r_num, r_den, _ptr(S_a), _ptr(S_hat),
+                               _ptr(S_exact if S_a is not None else None), _ptr(o), _p64(a_out), _p64(k_out),
+                               _ptr(ws), ws.numel(), _stream(stream, dev))
+    _check(rc, "gdn_tail_replay")
+    return {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o, "a": a_out.tolist(),
+            "k": k_out.tolist()}

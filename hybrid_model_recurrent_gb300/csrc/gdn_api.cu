@@ -1,0 +1,412 @@
+// gdn_api.cu - host side of the C ABI: argument validation, the exact index
+// plan (replay start, checkpoint selection), the ragged job table (longest job
+// first), TMA descriptors and kernel launches on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gdn_scan.h"
+#include "gdn_kernel.cuh"
+
+#define GDN_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+constexpr size_t kWorkspaceBytes = 256;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_d(int d) { return d == 32 || d == 64 || d == 128; }
+
+// [T, H, d] stream, box (box_x, 1, kChunk)
+bool make_stream_map(CUtensorMap* m, const void* base, bool bf16, int64_t T, int H, int d, int box_x) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const size_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(T, 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)(d * es), (cuuint64_t)((size_t)H * d * es)};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)gdn::kChunk};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Common validation of the problem description; fills seq lengths.
+gdn_status check_problem(const gdn_problem* p, std::vector<int64_t>& lens) {
+    if (!p || !p->cu_seqlens) return GDN_ERR_INVALID_ARG;
+    if (p->num_seqs < 1 || p->num_heads < 1 || p->d_k < 1 || p->d_v < 1) return GDN_ERR_INVALID_ARG;
+    if ((p->qkv_dtype != GDN_F32 && p->qkv_dtype != GDN_BF16) || (p->out_dtype != GDN_F32 && p->out_dtype != GDN_BF16))
+        return GDN_ERR_INVALID_ARG;
+    if (!supported_d(p->d_k) || !supported_d(p->d_v)) return GDN_ERR_UNSUPPORTED;
+    if (p->cu_seqlens[0] != 0) return GDN_ERR_INVALID_ARG;
+    lens.resize(p->num_seqs);
+    for (int b = 0; b < p->num_seqs; ++b) {
+        const int64_t n = p->cu_seqlens[b + 1] - p->cu_seqlens[b];
+        if (n < 0) return GDN_ERR_INVALID_ARG;
+        lens[b] = n;
+    }
+    const int64_t T = p->cu_seqlens[p->num_seqs];
+    if (T >= ((int64_t)1 << 31) - gdn::kChunk) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)p->num_heads * p->d_v * p->d_k > ((int64_t)1 << 40)) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)p->num_heads > (1 << 20)) return GDN_ERR_UNSUPPORTED;
+    return GDN_OK;
+}
+
+gdn_status check_streams(const gdn_problem* p, const void* q, const void* k, const void* v, const float* alpha,
+                         const float* beta, bool need_q, bool need_any) {
+    if (!need_any) return GDN_OK;
+    if (!k || !v || !alpha || !beta || (need_q && !q)) return GDN_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || (need_q && !aligned(q, 16))) return GDN_ERR_INVALID_ARG;
+    if (!aligned(alpha, 4) || !aligned(beta, 4)) return GDN_ERR_INVALID_ARG;
+    (void)p;
+    return GDN_OK;
+}
+
+gdn_status check_workspace(void* ws, size_t bytes) {
+    if (!ws || bytes < kWorkspaceBytes || !aligned(ws, 16)) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+// Validate one sequence's checkpoint list: strictly increasing in [1, n].
+bool ckpts_valid(const int64_t* c, int64_t M, int64_t n) {
+    for (int64_t i = 0; i < M; ++i) {
+        if (c[i] < 1 || c[i] > n) return false;
+        if (i > 0 && c[i] <= c[i - 1]) return false;
+    }
+    return true;
+}
+
+struct HostJob {
+    gdn::Job job;
+    std::vector<gdn::Ckpt> ckpts;
+};
+
+struct LaunchSpec {
+    const gdn_problem* p;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    void* o;
+    float* ckpt_states;
+    unsigned int* status;
+    bool readout;
+    bool twin;
+};
+
+// Sort jobs longest first and launch them in batches that fit one parameter block.
+gdn_status run_jobs(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_t stream) {
+    const gdn_problem* p = L.p;
+    const int H = p->num_heads, dv = p->d_v, dk = p->d_k;
+    const bool in_bf16 = p->qkv_dtype == GDN_BF16;
+    const bool out_bf16 = p->out_dtype == GDN_BF16;
+    const int wr = L.twin ? 16 : 32;               // real rows per consumer warp
+    const int nw = std::min(gdn::kMaxConsumerWarps, dv / wr);
+    const int rows = nw * wr;
+    const int ctas_per_head = dv / rows;
+    if (nw < 1 || rows * ctas_per_head != dv) return GDN_ERR_UNSUPPORTED;
+    if ((int64_t)H * ctas_per_head * gdn::kMaxJobs > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+
+    std::stable_sort(jobs.begin(), jobs.end(),
+                     [](const HostJob& a, const HostJob& b) { return a.job.len > b.job.len; });
+
+    const int64_t T = p->cu_seqlens[p->num_seqs];
+    auto prm = std::make_unique<gdn::Params>();
+    std::memset(prm.get(), 0, sizeof(gdn::Params));
+    // A map is encoded only for a stream that is given; the kernel issues no
+    // copy for a job without tokens, and streams are validated non-NULL whenever
+    // any job has tokens.
+    bool maps = true;
+    if (L.k) maps = maps && make_stream_map(&prm->tm_k, L.k, in_bf16, T, H, dk, dk);
+    if (L.readout && L.q) maps = maps && make_stream_map(&prm->tm_q, L.q, in_bf16, T, H, dk, dk);
+    if (L.v) maps = maps && make_stream_map(&prm->tm_v, L.v, in_bf16, T, H, dv, rows);
+    if (!maps) return GDN_ERR_CUDA;
+    prm->alpha = L.alpha;
+    prm->beta = L.beta;
+    prm->o = L.o;
+    prm->ckpt_states = L.ckpt_states;
+    prm->status = L.status;
+    prm->wait_limit_ns = g_wait_ns.load();
+    prm->H = H;
+    prm->dv = dv;
+    prm->nw = nw;
+    prm->rows_per_cta = rows;
+    prm->ctas_per_head = ctas_per_head;
+
+    const int idx = (((in_bf16 ? 1 : 0) * 2 + (out_bf16 ? 1 : 0)) * 2 + (L.readout ? 1 : 0)) * 2 + (L.twin ? 1 : 0);
+    gdn::LaunchFn fn = nullptr;
+    switch (dk) {
+        case 32: fn = gdn::launch_table<32>(idx); break;
+        case 64: fn = gdn::launch_table<64>(idx); break;
+        case 128: fn = gdn::launch_table<128>(idx); break;
+        default: return GDN_ERR_UNSUPPORTED;
+    }
+    if (!fn) return GDN_ERR_UNSUPPORTED;
+    const size_t smem = gdn::smem_bytes(dk, in_bf16 ? 2 : 4, rows, L.readout);
+
+    size_t i = 0;
+    while (i < jobs.size()) {
+        int nj = 0, nc = 0;
+        while (i + nj < jobs.size() && nj < gdn::kMaxJobs &&
+               nc + (int)jobs[i + nj].ckpts.size() <= gdn::kMaxCkpts) {
+            gdn::Job j = jobs[i + nj].job;
+            j.ck_begin = nc;
+            j.ck_count = (int32_t)jobs[i + nj].ckpts.size();
+            for (const gdn::Ckpt& c : jobs[i + nj].ckpts) prm->ckpts[nc++] = c;
+            prm->jobs[nj++] = j;
+        }
+        if (nj == 0) return GDN_ERR_UNSUPPORTED;  // one job with more checkpoints than a launch holds
+        prm->n_jobs = nj;
+        const int grid = nj * H * ctas_per_head;
+        cudaError_t e = fn(*prm, grid, smem, stream);
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        i += nj;
+    }
+    return GDN_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------
+// host-only helpers
+// ---------------------------------------------------------------------------------------
+GDN_EXPORT gdn_status gdn_replay_plan(int64_t m, int32_t r_num, int32_t r_den, int64_t* a, int64_t* k) {
+    if (!a || !k || m < 0 || m > ((int64_t)1 << 40) || r_den <= 0 || r_num < 0 || r_num > r_den)
+        return GDN_ERR_INVALID_ARG;
+    // k = ceil(r_num * m / r_den) in exact integers (no floating point)
+    const int64_t prod = (int64_t)r_num * m;
+    const int64_t q = prod / r_den;
+    const int64_t kk = q + ((q * r_den != prod) ? 1 : 0);
+    *k = kk;
+    *a = m - kk;
+    return GDN_OK;
+}
+
+GDN_EXPORT gdn_status gdn_select_ckpt(const int64_t* c, int32_t M, int64_t d, int32_t* j) {
+    if (!j || M < 0 || (M > 0 && !c)) return GDN_ERR_INVALID_ARG;
+    for (int32_t i = 1; i < M; ++i)
+        if (c[i] <= c[i - 1]) return GDN_ERR_INVALID_ARG;
+    // binary search for the last c_i <= d
+    int32_t lo = 0, hi = M;  // answer in [lo-1, hi-1]
+    while (lo < hi) {
+        const int32_t mid = lo + (hi - lo) / 2;
+        if (c[mid] <= d)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    *j = lo - 1;
+    return GDN_OK;
+}
+
+GDN_EXPORT size_t gdn_workspace_size(void) { return kWorkspaceBytes; }
+
+GDN_EXPORT void gdn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+GDN_EXPORT const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+GDN_EXPORT gdn_status gdn_clear_status(void* workspace, size_t ws_bytes, gdn_stream_t stream) {
+    gdn_status st = check_workspace(workspace, ws_bytes);
+    if (st != GDN_OK) return st;
+    return cudaMemsetAsync(workspace, 0, sizeof(unsigned int), (cudaStream_t)stream) == cudaSuccess ? GDN_OK
+                                                                                                     : GDN_ERR_CUDA;
+}
+
+GDN_EXPORT gdn_status gdn_read_status(const void* workspace, size_t ws_bytes, gdn_stream_t stream) {
+    gdn_status st = check_workspace(const_cast<void*>(workspace), ws_bytes);
+    if (st != GDN_OK) return st;
+    unsigned int word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+    return (word & gdn::STATUS_TIMEOUT) ? GDN_ERR_DEVICE_TIMEOUT : GDN_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// prefill with sparse checkpoints
+// ---------------------------------------------------------------------------------------
+GDN_EXPORT gdn_status gdn_prefill_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                       const float* alpha, const float* beta, const float* S0, void* o,
+                                       float* S_final, const int64_t* ckpt_pos, const int64_t* cu_ckpt,
+                                       float* ckpt_states, void* workspace, size_t ws_bytes, gdn_stream_t stream) {
+    std::vector<int64_t> lens;
+    gdn_status st = check_problem(p, lens);
+    if (st != GDN_OK) return st;
+    const int64_t T = p->cu_seqlens[p->num_seqs];
+    if ((st = check_streams(p, q, k, v, alpha, beta, o != nullptr, T > 0)) != GDN_OK) return st;
+    if ((st = check_workspace(workspace, ws_bytes)) != GDN_OK) return st;
+    if (!S_final || !aligned(S_final, 16) || (S0 && !aligned(S0, 16))) return GDN_ERR_INVALID_ARG;
+    if (o && !aligned(o, p->out_dtype == GDN_BF16 ? 2 : 4)) return GDN_ERR_INVALID_ARG;
+    const int B = p->num_seqs;
+    int64_t n_ck = 0;
+    if (cu_ckpt) {
+        if (cu_ckpt[0] != 0) return GDN_ERR_INVALID_ARG;
+        for (int b = 0; b < B; ++b)
+            if (cu_ckpt[b + 1] < cu_ckpt[b]) return GDN_ERR_INVALID_ARG;
+        n_ck = cu_ckpt[B];
+        if (n_ck > 0 && (!ckpt_pos || !ckpt_states || !aligned(ckpt_states, 16))) return GDN_ERR_INVALID_ARG;
+        for (int b = 0; b < B; ++b)
+            if (!ckpts_valid(ckpt_pos + cu_ckpt[b], cu_ckpt[b + 1] - cu_ckpt[b], lens[b])) return GDN_ERR_INVALID_ARG;
+        if (n_ck >= ((int64_t)1 << 23)) return GDN_ERR_UNSUPPORTED;
+    }
+    const size_t D = (size_t)p->num_heads * p->d_v * p->d_k;
+    std::vector<HostJob> jobs(B);
+    for (int b = 0; b < B; ++b) {
+        gdn::Job& j = jobs[b].job;
+        std::memset(&j, 0, sizeof(j));
+        j.tok_begin = p->cu_seqlens[b];
+        j.len = (int32_t)lens[b];
+        j.o_row_begin = o ? p->cu_seqlens[b] : -1;
+        j.s0 = S0 ? S0 + (size_t)b * D : nullptr;
+        j.s_final = S_final + (size_t)b * D;
+        if (cu_ckpt)
+            for (int64_t i = cu_ckpt[b]; i < cu_ckpt[b + 1]; ++i)
+                jobs[b].ckpts.push_back(gdn::Ckpt{(int32_t)ckpt_pos[i], (int32_t)i});
+    }
+    LaunchSpec L{p, q, k, v, alpha, beta, o, ckpt_states, static_cast<unsigned int*>(workspace), o != nullptr, false};
+    return run_jobs(L, jobs, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// resume from the deepest checkpoint at or below d
+// ---------------------------------------------------------------------------------------
+GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                           const float* alpha, const float* beta, const float* S0,
+                                           const float* ckpt_states, const int64_t* ckpt_pos,
+                                           const int64_t* cu_ckpt, int32_t num_probes, const int32_t* probe_seq,
+                                           const int64_t* probe_depth, float* S_out, void* o_out,
+                                           int64_t* chosen_pos, int64_t* o_offsets, void* workspace,
+                                           size_t ws_bytes, gdn_stream_t stream) {
+    std::vector<int64_t> lens;
+    gdn_status st = check_problem(p, lens);
+    if (st != GDN_OK) return st;
+    if (num_probes < 0) return GDN_ERR_INVALID_ARG;
+    if (num_probes > 0 && (!probe_seq || !probe_depth || !S_out || !aligned(S_out, 16))) return GDN_ERR_INVALID_ARG;
+    if ((st = check_workspace(workspace, ws_bytes)) != GDN_OK) return st;
+    if (S0 && !aligned(S0, 16)) return GDN_ERR_INVALID_ARG;
+    if (o_out && !aligned(o_out, p->out_dtype == GDN_BF16 ? 2 : 4)) return GDN_ERR_INVALID_ARG;
+    const int B = p->num_seqs;
+    if (cu_ckpt) {
+        if (cu_ckpt[0] != 0) return GDN_ERR_INVALID_ARG;
+        for (int b = 0; b < B; ++b)
+            if (cu_ckpt[b + 1] < cu_ckpt[b]) return GDN_ERR_INVALID_ARG;
+        if (cu_ckpt[B] > 0 && (!ckpt_pos || !ckpt_states || !aligned(ckpt_states, 16))) return GDN_ERR_INVALID_ARG;
+        for (int b = 0; b < B; ++b)
+            if (!ckpts_valid(ckpt_pos + cu_ckpt[b], cu_ckpt[b + 1] - cu_ckpt[b], lens[b])) return GDN_ERR_INVALID_ARG;
+    }
+    const size_t D = (size_t)p->num_heads * p->d_v * p->d_k;
+    std::vector<HostJob> jobs(num_probes);
+    std::vector<int64_t> chosen(num_probes), offs(num_probes + 1, 0);
+    int64_t total = 0;
+    for (int32_t i = 0; i < num_probes; ++i) {
+        const int s = probe_seq[i];
+        const int64_t d = probe_depth[i];
+        if (s < 0 || s >= B || d < 0 || d > lens[s]) return GDN_ERR_INVALID_ARG;
+        int32_t j = -1;
+        if (cu_ckpt && cu_ckpt[s + 1] > cu_ckpt[s]) {
+            if (gdn_select_ckpt(ckpt_pos + cu_ckpt[s], (int32_t)(cu_ckpt[s + 1] - cu_ckpt[s]), d, &j) != GDN_OK)
+                return GDN_ERR_INVALID_ARG;
+        }
+        const int64_t c = j < 0 ? 0 : ckpt_pos[cu_ckpt[s] + j];
+        chosen[i] = c;
+        offs[i] = total;
+        total += d - c;
+        gdn::Job& jb = jobs[i].job;
+        std::memset(&jb, 0, sizeof(jb));
+        jb.tok_begin = p->cu_seqlens[s] + c;
+        jb.len = (int32_t)(d - c);
+        jb.o_row_begin = o_out ? offs[i] : -1;
+        jb.s0 = j < 0 ? (S0 ? S0 + (size_t)s * D : nullptr) : ckpt_states + (size_t)(cu_ckpt[s] + j) * D;
+        jb.s_final = S_out + (size_t)i * D;
+    }
+    offs[num_probes] = total;
+    if ((st = check_streams(p, q, k, v, alpha, beta, o_out != nullptr, total > 0)) != GDN_OK) return st;
+    if (chosen_pos) std::copy(chosen.begin(), chosen.end(), chosen_pos);
+    if (o_offsets) std::copy(offs.begin(), offs.end(), o_offsets);
+    if (num_probes == 0) return GDN_OK;
+    LaunchSpec L{p, q, k, v, alpha, beta, o_out, nullptr, static_cast<unsigned int*>(workspace), o_out != nullptr,
+                 false};
+    return run_jobs(L, jobs, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// Tail-Replay
+// ---------------------------------------------------------------------------------------
+GDN_EXPORT gdn_status gdn_tail_replay(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                      const float* alpha, const float* beta, const int64_t* m, int32_t r_num,
+                                      int32_t r_den, const float* S_a, float* S_hat, float* S_exact, void* o,
+                                      int64_t* a_out, int64_t* k_out, void* workspace, size_t ws_bytes,
+                                      gdn_stream_t stream) {
+    std::vector<int64_t> lens;
+    gdn_status st = check_problem(p, lens);
+    if (st != GDN_OK) return st;
+    if (!m || !S_hat || !aligned(S_hat, 16)) return GDN_ERR_INVALID_ARG;
+    if ((S_a == nullptr) != (S_exact == nullptr)) return GDN_ERR_INVALID_ARG;
+    if (S_a && (!aligned(S_a, 16) || !aligned(S_exact, 16))) return GDN_ERR_INVALID_ARG;
+    if (o && !aligned(o, p->out_dtype == GDN_BF16 ? 2 : 4)) return GDN_ERR_INVALID_ARG;
+    if ((st = check_workspace(workspace, ws_bytes)) != GDN_OK) return st;
+    const int B = p->num_seqs;
+    const size_t D = (size_t)p->num_heads * p->d_v * p->d_k;
+    std::vector<HostJob> jobs(B);
+    std::vector<int64_t> av(B), kv(B);
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b) {
+        if (m[b] < 0 || m[b] > lens[b]) return GDN_ERR_INVALID_ARG;
+        if (gdn_replay_plan(m[b], r_num, r_den, &av[b], &kv[b]) != GDN_OK) return GDN_ERR_INVALID_ARG;
+        total += kv[b];
+        gdn::Job& j = jobs[b].job;
+        std::memset(&j, 0, sizeof(j));
+        j.tok_begin = p->cu_seqlens[b] + av[b];
+        j.len = (int32_t)kv[b];
+        j.o_row_begin = o ? p->cu_seqlens[b] + av[b] : -1;
+        j.s0 = nullptr;
+        j.s0_twin = S_a ? S_a + (size_t)b * D : nullptr;
+        j.s_final = S_hat + (size_t)b * D;
+        j.s_final_twin = S_exact ? S_exact + (size_t)b * D : nullptr;
+    }
+    if ((st = check_streams(p, q, k, v, alpha, beta, o != nullptr, total > 0)) != GDN_OK) return st;
+    if (a_out) std::copy(av.begin(), av.end(), a_out);
+    if (k_out) std::copy(kv.begin(), kv.end(), k_out);
+    LaunchSpec L{p, q, k, v, alpha, beta, o, nullptr, static_cast<unsigned int*>(workspace), o != nullptr,
+                 S_a != nullptr};
+    return run_jobs(L, jobs, (cudaStream_t)stream);
+}

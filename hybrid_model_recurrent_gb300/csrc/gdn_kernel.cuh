@@ -1,0 +1,548 @@
+// gdn_kernel.cuh - sm_103a state-scan kernel for the Gated DeltaNet recurrence.
+//
+// Operation (notes page "Tail-Replay: Escaping the Curse of Linear Attention in
+// Prefix Caching for Hybrid LLMs", section 2.3, equation (1), right-multiplied
+// for S in R^{d_v x d_k}):
+//     u = S_{t-1} k_t,  w = beta_t (v_t - alpha_t u),  S_t = alpha_t S_{t-1} + w k_t^T,
+//     o_t = S_t q_t.
+// (alpha S (I - beta k k^T) + beta v k^T expands to exactly this.)
+//
+// Design (one CTA = one (job, head, block of state rows)):
+//  * Row i of S evolves only from v_{t,i}: the key-space operator acts from the
+//    right, so the rows of a head split across lanes, warps and CTAs with no
+//    exchange.  Each consumer warp owns 32 state rows ("slots"); a lane holds an
+//    R x C register tile (R = C-lanes per row group, R*C = d_k), so the dot
+//    products S k and S q reduce over NCL lanes with a reduce-scatter that leaves
+//    lane `cl` holding the full sums of slot `cl`.
+//  * The state is kept in a running scale: S = s * St.  With s_t = alpha_t s_{t-1}
+//    the update becomes St += c k^T with c = (beta/s_t) v - beta (St_{t-1} k), so
+//    each state element costs exactly three FMAs per token (update, S k, S q),
+//    issued as packed fp32x2 FMAs.  The producer warp computes s_t and beta/s_t
+//    per token (sequential left-to-right product) and schedules renormalisation
+//    (St *= s, s = 1) whenever the scale would fall below 2^-32, at every
+//    checkpoint and after the last token, so dumps and results are plain states
+//    and the arithmetic after a checkpoint does not depend on the path before it.
+//  * One producer warp stages k, q, v tiles of 32 tokens with TMA into a 4-deep
+//    shared-memory ring guarded by mbarriers; consumers widen bf16 to fp32 on
+//    load.  Every wait is bounded by a wall-clock limit; on expiry the kernel
+//    records GDN device status and returns (never hangs).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+namespace gdn {
+
+constexpr int kChunk = 32;     // tokens per pipeline stage
+constexpr int kStages = 4;     // depth of the shared-memory ring
+constexpr int kMaxJobs = 256;  // jobs per launch (host splits larger batches)
+constexpr int kMaxCkpts = 1536;
+constexpr int kMaxConsumerWarps = 4;
+constexpr float kRenormFloor = 0x1p-32f;
+
+enum : uint32_t { FLAG_RENORM = 1u, FLAG_DUMP = 2u, FLAG_INDEX_SHIFT = 8u };
+enum : unsigned { STATUS_TIMEOUT = 1u };
+
+// One scan over a contiguous token range, the same for all heads.
+struct Job {
+    int64_t tok_begin;      // absolute stream row of the job's first token
+    int64_t o_row_begin;    // absolute output row of the first token; -1: no readout
+    const float* s0;        // [H, dv, dk] initial state, nullptr = zeros
+    const float* s0_twin;   // [H, dv, dk] initial state of the twin (twin kernels)
+    float* s_final;         // [H, dv, dk] state after the last token
+    float* s_final_twin;    // [H, dv, dk] twin state after the last token
+    int32_t len;            // tokens
+    int32_t ck_begin;       // first entry of the launch's checkpoint table
+    int32_t ck_count;       // entries for this job
+    int32_t pad_;
+};
+static_assert(sizeof(Job) == 64, "Job layout");
+
+struct Ckpt {
+    int32_t pos;   // 1-based token position within the job
+    int32_t slot;  // destination slot in ckpt_states ([slot, H, dv, dk])
+};
+
+struct Params {
+    CUtensorMap tm_q;   // [T, H, dk] box (dk, 1, kChunk)
+    CUtensorMap tm_k;   // [T, H, dk] box (dk, 1, kChunk)
+    CUtensorMap tm_v;   // [T, H, dv] box (rows_per_cta, 1, kChunk)
+    const float* alpha; // [T, H]
+    const float* beta;  // [T, H]
+    void* o;            // [rows, H, dv]
+    float* ckpt_states; // [slots, H, dv, dk]
+    unsigned int* status;
+    unsigned long long wait_limit_ns;
+    int32_t H;
+    int32_t dv;
+    int32_t nw;             // consumer warps per CTA
+    int32_t rows_per_cta;   // real state rows per CTA
+    int32_t ctas_per_head;  // dv / rows_per_cta
+    int32_t n_jobs;
+    Job jobs[kMaxJobs];
+    Ckpt ckpts[kMaxCkpts];
+};
+
+// ------------------------------------------------------------------------------------
+// PTX helpers
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, "
+        "p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `parity` to complete, for at most limit_ns.  Called by
+// all 32 lanes of a warp; the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_ns();
+        while (!(ok = mbar_try_wait(bar, parity))) {
+            if (global_ns() - t0 > limit_ns) break;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Reduce-scatter over the NCL lanes of a row group: on entry v[i] is this lane's
+// partial sum for slot i; on exit the return value is the full sum of slot
+// (lane & (NCL-1)).
+template <int RT>
+__device__ __forceinline__ float reduce_scatter(float (&v)[RT], int lane) {
+#pragma unroll
+    for (int half = RT / 2; half >= 1; half >>= 1) {
+        const bool up = (lane & half) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        }
+    }
+    return v[0];
+}
+
+// Shared-memory layout of one pipeline stage.
+struct StageLayout {
+    uint32_t k_off, q_off, v_off, sc_off, bytes, tx_bytes;
+};
+__host__ __device__ constexpr uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
+__host__ __device__ inline StageLayout stage_layout(int dk, int in_bytes, int rows, bool readout) {
+    StageLayout L{};
+    const uint32_t kb = (uint32_t)(kChunk * dk * in_bytes);
+    const uint32_t vb = (uint32_t)(kChunk * rows * in_bytes);
+    L.k_off = 0;
+    L.q_off = align128(kb);
+    L.v_off = L.q_off + (readout ? align128(kb) : 0u);
+    L.sc_off = L.v_off + align128(vb);
+    L.bytes = align128(L.sc_off + kChunk * 16u);
+    L.tx_bytes = kb * (readout ? 2u : 1u) + vb;
+    return L;
+}
+__host__ __device__ inline uint32_t smem_bytes(int dk, int in_bytes, int rows, bool readout) {
+    return stage_layout(dk, in_bytes, rows, readout).bytes * kStages + 2u * kStages * 8u + 128u;
+}
+
+// ------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------
+template <int DK, bool IN_BF16, bool OUT_BF16, bool READOUT, bool TWIN>
+__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
+    gdn_scan_kernel(const __grid_constant__ Params p) {
+    constexpr int ES = IN_BF16 ? 2 : 4;
+    constexpr int NCL = DK >= 64 ? 8 : 4;    // lanes sharing one row group
+    constexpr int RT = NCL;                  // row slots per lane
+    constexpr int CT = DK / NCL;             // columns per lane
+    constexpr int CT2 = CT / 2;
+    constexpr int CH = 16 / ES;              // elements per 16-byte chunk
+    constexpr int NCH = CT / CH;             // chunks per lane per row
+    constexpr int NRG = 32 / NCL;            // row groups per warp
+    constexpr int HALF = TWIN ? RT / 2 : RT; // real rows per lane per state
+    constexpr int WR = NRG * HALF;           // real rows per warp
+    static_assert(NCH >= 1 && CT % CH == 0 && CT % 2 == 0, "lane tile");
+    using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127u) & ~uintptr_t(127));
+
+    const int nw = p.nw;
+    const int RB = p.rows_per_cta;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const StageLayout L = stage_layout(DK, ES, RB, READOUT);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bytes * kStages);
+    uint64_t* empty = full + kStages;
+
+    const int per_job = p.H * p.ctas_per_head;
+    const int job_idx = blockIdx.x / per_job;
+    const int rem = blockIdx.x - job_idx * per_job;
+    const int h = rem / p.ctas_per_head;
+    const int rb = rem - h * p.ctas_per_head;
+    const int64_t tok_begin = p.jobs[job_idx].tok_begin;
+    const int len = p.jobs[job_idx].len;
+    const int nchunks = (len + kChunk - 1) / kChunk;
+    const uint64_t limit = p.wait_limit_ns;
+    const int H = p.H;
+    const int dv = p.dv;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], (uint32_t)nw);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == nw) {
+        // ============================== producer warp ==============================
+        const size_t gate0 = (size_t)tok_begin * (size_t)H + (size_t)h;
+        const int ck_end = p.jobs[job_idx].ck_begin + p.jobs[job_idx].ck_count;
+        int ck_cur = p.jobs[job_idx].ck_begin;
+        float s_carry = 1.0f;
+        int issued = 0;
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int st = c % kStages;
+            if (c >= kStages && !warp_wait(&empty[st], (uint32_t)(((c / kStages) + 1) & 1), limit)) {
+                ok = false;
+                break;
+            }
+            unsigned char* stage = smem + (size_t)st * L.bytes;
+            if (lane == 0) {
+                mbar_expect_tx(&full[st], L.tx_bytes);
+                const int t0 = (int)(tok_begin + (int64_t)c * kChunk);
+                tma_load_3d(stage + L.k_off, &p.tm_k, 0, h, t0, &full[st]);
+                if (READOUT) tma_load_3d(stage + L.q_off, &p.tm_q, 0, h, t0, &full[st]);
+                tma_load_3d(stage + L.v_off, &p.tm_v, rb * RB, h, t0, &full[st]);
+            }
+            issued = c + 1;
+            const int base = c * kChunk;
+            const int tau = base + lane;
+            float a = 1.0f, b = 0.0f;
+            if (tau < len) {
+                a = __ldg(p.alpha + gate0 + (size_t)tau * (size_t)H);
+                b = __ldg(p.beta + gate0 + (size_t)tau * (size_t)H);
+            }
+            float a_look = 1.0f;
+            if (base + kChunk < len) a_look = __ldg(p.alpha + gate0 + (size_t)(base + kChunk) * (size_t)H);
+            uint32_t fl = 0;
+            while (ck_cur < ck_end && p.ckpts[ck_cur].pos <= base + kChunk) {
+                if (p.ckpts[ck_cur].pos - 1 == tau)
+                    fl = FLAG_DUMP | FLAG_RENORM | ((uint32_t)ck_cur << FLAG_INDEX_SHIFT);
+                ++ck_cur;
+            }
+            if (tau == len - 1) fl |= FLAG_RENORM;
+            // running scale, left to right (chunk-boundary independent)
+            float s = s_carry, my_s = 1.0f;
+            uint32_t my_fl = fl;
+#pragma unroll 4
+            for (int j = 0; j < kChunk; ++j) {
+                const float aj = __shfl_sync(0xffffffffu, a, j);
+                const float an_sh = __shfl_sync(0xffffffffu, a, (j + 1) & 31);
+                const uint32_t fj = __shfl_sync(0xffffffffu, fl, j);
+                const float an = (j + 1 < kChunk) ? an_sh : a_look;
+                s = s * aj;
+                const bool valid = base + j < len;
+                const bool ren =
+                    valid && ((fj & FLAG_RENORM) != 0u || (base + j + 1 < len && s * an < kRenormFloor));
+                if (lane == j) {
+                    my_s = s;
+                    my_fl = fj | (ren ? FLAG_RENORM : 0u);
+                }
+                if (ren) s = 1.0f;
+            }
+            s_carry = s;
+            const float b1 = __fdiv_rn(b, my_s);
+            reinterpret_cast<float4*>(stage + L.sc_off)[lane] = make_float4(my_s, b1, b, __uint_as_float(my_fl));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[st]);
+        }
+        // never leave with copies in flight into this CTA's shared memory
+        for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
+            warp_wait(&full[c % kStages], (uint32_t)((c / kStages) & 1), limit);
+        if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
+        return;
+    }
+
+    // ================================ consumer warps ===============================
+    const int cl = lane & (NCL - 1);
+    const int rg = lane / NCL;
+    const int my_state = TWIN ? (cl / HALF) : 0;
+    const int my_row = warp * WR + rg * HALF + (TWIN ? (cl % HALF) : cl);  // CTA-relative real row
+    const int grow_base = rb * RB + warp * WR + rg * HALF;                  // head row of slot 0
+    const size_t head_state = (size_t)h * (size_t)dv * DK;
+
+    float2 S[RT][CT2];
+    {
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            const int state = TWIN ? (i / HALF) : 0;
+            const int grow = grow_base + (TWIN ? (i % HALF) : i);
+            const float* src = state == 0 ? p.jobs[job_idx].s0 : p.jobs[job_idx].s0_twin;
+#pragma unroll
+            for (int jc = 0; jc < NCH; ++jc) {
+                const int col0 = (cl + NCL * jc) * CH;
+#pragma unroll
+                for (int e4 = 0; e4 < CH / 4; ++e4) {
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (src) x = __ldg(reinterpret_cast<const float4*>(src + head_state + (size_t)grow * DK + col0) + e4);
+                    S[i][jc * (CH / 2) + e4 * 2 + 0] = make_float2(x.x, x.y);
+                    S[i][jc * (CH / 2) + e4 * 2 + 1] = make_float2(x.z, x.w);
+                }
+            }
+        }
+    }
+
+    auto load_vec = [&](const unsigned char* tok, float2 (&dst)[CT2]) {
+        const uint4* p4 = reinterpret_cast<const uint4*>(tok);
+#pragma unroll
+        for (int jc = 0; jc < NCH; ++jc) {
+            const uint4 w = p4[cl + NCL * jc];
+            if constexpr (IN_BF16) {
+                dst[jc * 4 + 0] = bf16x2_to_float2(w.x);
+                dst[jc * 4 + 1] = bf16x2_to_float2(w.y);
+                dst[jc * 4 + 2] = bf16x2_to_float2(w.z);
+                dst[jc * 4 + 3] = bf16x2_to_float2(w.w);
+            } else {
+                dst[jc * 2 + 0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+                dst[jc * 2 + 1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+            }
+        }
+    };
+    auto load_v = [&](const unsigned char* stage, int tau) -> float {
+        const unsigned char* pv = stage + L.v_off + ((size_t)tau * RB + my_row) * ES;
+        if constexpr (IN_BF16)
+            return __uint_as_float(((uint32_t) * reinterpret_cast<const unsigned short*>(pv)) << 16);
+        else
+            return *reinterpret_cast<const float*>(pv);
+    };
+    auto dot_k = [&](const float2 (&kv)[CT2], float (&out)[RT]) {
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < CT2; ++jj) acc = __ffma2_rn(S[i][jj], kv[jj], acc);
+            out[i] = acc.x + acc.y;
+        }
+    };
+    auto broadcast_c = [&](float c_mine, float (&creg)[RT]) {
+        const int grp = lane & ~(NCL - 1);
+#pragma unroll
+        for (int i = 0; i < RT; ++i) creg[i] = __shfl_sync(0xffffffffu, c_mine, grp | i);
+    };
+
+    bool ok = true;
+    float creg[RT];
+    float2 kc[CT2];
+#pragma unroll
+    for (int i = 0; i < RT; ++i) creg[i] = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < CT2; ++jj) kc[jj] = make_float2(0.f, 0.f);
+
+    if (len > 0) {
+        ok = warp_wait(&full[0], 0u, limit);
+        if (ok) {
+            load_vec(smem + L.k_off, kc);
+            float pk[RT];
+            dot_k(kc, pk);
+            const float pkr = reduce_scatter<RT>(pk, lane);
+            const float4 sc = reinterpret_cast<const float4*>(smem + L.sc_off)[0];
+            const float vv = load_v(smem, 0);
+            broadcast_c(sc.y * vv - sc.z * pkr, creg);
+        }
+    }
+
+    const int64_t o_row0 = p.jobs[job_idx].o_row_begin;
+    for (int tg = 0; ok && tg < len; ++tg) {
+        const int c = tg / kChunk;
+        const int tau = tg - c * kChunk;
+        const int st = c % kStages;
+        const bool has_next = tg + 1 < len;
+        const int cn = (tg + 1) / kChunk;
+        const int taun = tg + 1 - cn * kChunk;
+        const int stn = cn % kStages;
+        unsigned char* stage = smem + (size_t)st * L.bytes;
+        unsigned char* stage_n = smem + (size_t)stn * L.bytes;
+        if (has_next && taun == 0) {
+            if (!warp_wait(&full[stn], (uint32_t)((cn / kStages) & 1), limit)) {
+                ok = false;
+                break;
+            }
+        }
+        float2 kn[CT2];
+        if (has_next) {
+            load_vec(stage_n + L.k_off + (size_t)taun * DK * ES, kn);
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < CT2; ++jj) kn[jj] = make_float2(0.f, 0.f);
+        }
+        // pass A: St += c k_t^T, then the next token's St k_{t+1}
+        float pk[RT];
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            const float2 cc = make_float2(creg[i], creg[i]);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int jj = 0; jj < CT2; ++jj) {
+                S[i][jj] = __ffma2_rn(cc, kc[jj], S[i][jj]);
+                acc = __ffma2_rn(S[i][jj], kn[jj], acc);
+            }
+            pk[i] = acc.x + acc.y;
+        }
+        float pkr = reduce_scatter<RT>(pk, lane);
+        const float4 sct = reinterpret_cast<const float4*>(stage + L.sc_off)[tau];
+        if constexpr (READOUT) {
+            // pass B: readout St q_t of the post-update state
+            float2 qv[CT2];
+            load_vec(stage + L.q_off + (size_t)tau * DK * ES, qv);
+            float pq[RT];
+            dot_k(qv, pq);
+            const float pqr = reduce_scatter<RT>(pq, lane);
+            if (o_row0 >= 0 && my_state == 0) {
+                const float ov = sct.x * pqr;
+                OutT* op = reinterpret_cast<OutT*>(p.o) + ((size_t)(o_row0 + tg) * (size_t)H + (size_t)h) * (size_t)dv +
+                           (size_t)(rb * RB + my_row);
+                if constexpr (OUT_BF16)
+                    *op = __float2bfloat16_rn(ov);
+                else
+                    *op = ov;
+            }
+        }
+        const uint32_t fl = __float_as_uint(sct.w);
+        if (fl & FLAG_RENORM) {
+            const float2 ss = make_float2(sct.x, sct.x);
+#pragma unroll
+            for (int i = 0; i < RT; ++i)
+#pragma unroll
+                for (int jj = 0; jj < CT2; ++jj) S[i][jj] = __fmul2_rn(S[i][jj], ss);
+            if (has_next) {
+                dot_k(kn, pk);
+                pkr = reduce_scatter<RT>(pk, lane);
+            }
+            if (fl & FLAG_DUMP) {
+                const int slot = p.ckpts[fl >> FLAG_INDEX_SHIFT].slot;
+                float* dst = p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state;
+#pragma unroll
+                for (int i = 0; i < RT; ++i) {
+                    const int grow = grow_base + (TWIN ? (i % HALF) : i);
+                    if (TWIN && i >= HALF) continue;
+#pragma unroll
+                    for (int jc = 0; jc < NCH; ++jc) {
+                        const int col0 = (cl + NCL * jc) * CH;
+#pragma unroll
+                        for (int e4 = 0; e4 < CH / 4; ++e4) {
+                            const float2 a0 = S[i][jc * (CH / 2) + e4 * 2 + 0];
+                            const float2 a1 = S[i][jc * (CH / 2) + e4 * 2 + 1];
+                            reinterpret_cast<float4*>(dst + (size_t)grow * DK + col0)[e4] =
+                                make_float4(a0.x, a0.y, a1.x, a1.y);
+                        }
+                    }
+                }
+            }
+        }
+        if (has_next) {
+            const float4 scn = reinterpret_cast<const float4*>(stage_n + L.sc_off)[taun];
+            const float vv = load_v(stage_n, taun);
+            broadcast_c(scn.y * vv - scn.z * pkr, creg);
+#pragma unroll
+            for (int jj = 0; jj < CT2; ++jj) kc[jj] = kn[jj];
+        }
+        if (tau == kChunk - 1 || !has_next) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+    }
+
+    if (!ok) {
+        if (lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
+        return;
+    }
+    // final state(s): the last token always renormalises, so St is the state
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+        const int state = TWIN ? (i / HALF) : 0;
+        const int grow = grow_base + (TWIN ? (i % HALF) : i);
+        float* dst = (state == 0 ? p.jobs[job_idx].s_final : p.jobs[job_idx].s_final_twin);
+        if (!dst) continue;
+        dst += head_state;
+#pragma unroll
+        for (int jc = 0; jc < NCH; ++jc) {
+            const int col0 = (cl + NCL * jc) * CH;
+#pragma unroll
+            for (int e4 = 0; e4 < CH / 4; ++e4) {
+                const float2 a0 = S[i][jc * (CH / 2) + e4 * 2 + 0];
+                const float2 a1 = S[i][jc * (CH / 2) + e4 * 2 + 1];
+                reinterpret_cast<float4*>(dst + (size_t)grow * DK + col0)[e4] = make_float4(a0.x, a0.y, a1.x, a1.y);
+            }
+        }
+    }
+}
+
+// Launch one kernel instance; instantiated per d_k in inst_dk*.cu.
+template <int DK, bool IN_BF16, bool OUT_BF16, bool READOUT, bool TWIN>
+cudaError_t launch_scan(const Params& p, int grid, size_t smem, cudaStream_t stream) {
+    auto kern = gdn_scan_kernel<DK, IN_BF16, OUT_BF16, READOUT, TWIN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 32 * (p.nw + 1), smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+using LaunchFn = cudaError_t (*)(const Params&, int, size_t, cudaStream_t);
+
+// index: ((in_bf16 * 2 + out_bf16) * 2 + readout) * 2 + twin
+template <int DK>
+LaunchFn launch_table(int idx);
+template <>
+LaunchFn launch_table<32>(int idx);
+template <>
+LaunchFn launch_table<64>(int idx);
+template <>
+LaunchFn launch_table<128>(int idx);
+
+}  // namespace gdn

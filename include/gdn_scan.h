@@ -1,0 +1,192 @@
+/*
+ * gdn_scan.h - C ABI of the GB300 (sm_103a) Gated DeltaNet state-scan library.
+ *
+ * The operation (notes page "Tail-Replay: Escaping the Curse of Linear
+ * Attention in Prefix Caching for Hybrid LLMs", section 2.3, equation (1),
+ * in the right-multiplied layout the same section requires for a state
+ * S in R^{d_v x d_k}):
+ *
+ *     S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t                      (readout of the post-update state)
+ *
+ * run independently for every (sequence, head) of a ragged batch.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Token streams are packed over the batch: q, k are [T, H, d_k], v is
+ *    [T, H, d_v], alpha and beta are [T, H] fp32, all row-major (last index
+ *    fastest), where T = cu_seqlens[B] and sequence b owns rows
+ *    [cu_seqlens[b], cu_seqlens[b+1]).  q/k/v are fp32 or bf16 (qkv_dtype);
+ *    bf16 values are widened exactly to fp32.
+ *  - States are fp32 [d_v, d_k] row-major (key index fastest), stacked as
+ *    [.., H, d_v, d_k].  All arithmetic is fp32.
+ *  - Positions are 1-based as on the pages: "token t" is row t-1 of its
+ *    sequence; "the state at c" is the state after token c.
+ *  - Device pointers must be 16-byte aligned (q, k, v, states) or aligned
+ *    to their element size (alpha, beta, o).  Host arrays are read before the
+ *    call returns.  Device work is enqueued on `stream` (NULL = the legacy
+ *    default stream) and is complete when the stream is; outputs are valid
+ *    only then.
+ *  - The caller owns every buffer.  The library allocates no device memory;
+ *    it needs a small caller-provided workspace (gdn_workspace_size bytes,
+ *    16-byte aligned) that carries a sticky device status word.
+ *  - Errors: a non-GDN_OK status.  Invalid arguments are detected on the
+ *    host before anything is enqueued; outputs are then untouched.  A
+ *    kernel-side failure (a bounded wait that ran out) is reported later by
+ *    gdn_read_status on the same workspace.
+ *  - Supported sizes: d_k, d_v in {32, 64, 128}; T < 2^31; H * d_v * d_k
+ *    state elements per sequence fit in 2^40.  alpha must lie in (0, 1]
+ *    (results are exact to fp32 rounding for alpha >= 1e-30), beta is any
+ *    finite value.
+ */
+#ifndef GDN_SCAN_H
+#define GDN_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,    /* bad pointer, size, position or alignment      */
+    GDN_ERR_UNSUPPORTED = 2,    /* valid but not supported (e.g. d_k = 96)        */
+    GDN_ERR_CUDA = 3,           /* a CUDA runtime / driver call failed            */
+    GDN_ERR_DEVICE_TIMEOUT = 4  /* a kernel's bounded wait ran out (see read_status) */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef struct gdn_problem {
+    int32_t num_seqs;            /* B >= 1                                           */
+    int32_t num_heads;           /* H >= 1                                           */
+    int32_t d_k;                 /* key / query width                                */
+    int32_t d_v;                 /* value width = rows of the state                  */
+    const int64_t* cu_seqlens;   /* host [B+1]: 0 = cu[0] <= cu[1] <= ... = T        */
+    gdn_dtype qkv_dtype;         /* dtype of q, k, v                                 */
+    gdn_dtype out_dtype;         /* dtype of the readout o (rounded to nearest even) */
+} gdn_problem;
+
+/*
+ * Prefill with sparse exact checkpoints.
+ * ("Sparse prefix caching in hybrid and recurrent LLM serving", section 3:
+ * exact recurrent states are stored at positions 1 <= c_1 < ... < c_M <= N.)
+ *
+ * For every sequence b and head h, scan tokens 1..N_b from S0[b, h] (zeros
+ * when S0 is NULL), write the readout of every token to o (skipped when o is
+ * NULL), dump the state after each checkpoint position and write the state
+ * after token N_b to S_final.
+ *
+ *  q            device [T, H, d_k]   (may be NULL when o is NULL)
+ *  k            device [T, H, d_k]
+ *  v            device [T, H, d_v]
+ *  alpha, beta  device [T, H] fp32
+ *  S0           device [B, H, d_v, d_k] fp32, or NULL for zero initial states
+ *  o            device [T, H, d_v] out_dtype, or NULL
+ *  S_final      device [B, H, d_v, d_k] fp32
+ *  ckpt_pos     host, concatenated per sequence: the M_b positions of sequence
+ *               b are ckpt_pos[cu_ckpt[b] .. cu_ckpt[b+1]), strictly
+ *               increasing, each in [1, N_b]
+ *  cu_ckpt      host [B+1], cu_ckpt[0] = 0, non-decreasing (NULL = no checkpoints)
+ *  ckpt_states  device [cu_ckpt[B], H, d_v, d_k] fp32: slot cu_ckpt[b] + i
+ *               receives the state after token ckpt_pos[cu_ckpt[b] + i]
+ */
+gdn_status gdn_prefill_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
+                            const float* alpha, const float* beta, const float* S0, void* o,
+                            float* S_final, const int64_t* ckpt_pos, const int64_t* cu_ckpt,
+                            float* ckpt_states, void* workspace, size_t ws_bytes,
+                            gdn_stream_t stream);
+
+/*
+ * Resume from the deepest stored checkpoint.
+ * ("Sparse prefix caching ...", section 3: for overlap depth d take
+ * j = argmax{c_i <= d}, restore S_{c_j}, recompute tokens c_j+1 .. d; nothing
+ * to recompute when c_j = d.)  With no checkpoint at or below d the scan
+ * starts from the initial state S0[s] (zeros when S0 is NULL), i.e. c_0 = 0.
+ *
+ *  q, k, v, alpha, beta   the packed streams of gdn_prefill_ckpt
+ *  S0           device [B, H, d_v, d_k] or NULL (the c_0 = 0 state)
+ *  ckpt_states, ckpt_pos, cu_ckpt   as written / read by gdn_prefill_ckpt
+ *  num_probes   P >= 0
+ *  probe_seq    host [P]: sequence of each probe, in [0, B)
+ *  probe_depth  host [P]: overlap depth d in [0, N_seq]
+ *  S_out        device [P, H, d_v, d_k]: state after token d
+ *  o_out        device [R, H, d_v] out_dtype or NULL: readout of the
+ *               recomputed tokens, probe p's tokens c_j+1..d packed at rows
+ *               [o_offsets[p], o_offsets[p+1]) in probe order,
+ *               R = sum_p (d_p - c_jp)
+ *  chosen_pos   host [P] out (nullable): c_j of each probe (0 = initial state)
+ *  o_offsets    host [P+1] out (nullable): the packing offsets above
+ */
+gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                const float* alpha, const float* beta, const float* S0,
+                                const float* ckpt_states, const int64_t* ckpt_pos,
+                                const int64_t* cu_ckpt, int32_t num_probes,
+                                const int32_t* probe_seq, const int64_t* probe_depth, float* S_out,
+                                void* o_out, int64_t* chosen_pos, int64_t* o_offsets,
+                                void* workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/*
+ * Tail-Replay state recovery.
+ * (Tail-Replay notes page, section 2.1 table: k = ceil(r m), a = m - k;
+ * section 2.2 steps 2-3: set the state to zero at the tail start and run the
+ * k tail tokens, i.e. positions a+1 .. m, giving the approximation S_hat_m.)
+ *
+ *  q, k, v, alpha, beta   full prefix streams; only rows [cu[b]+a_b, cu[b]+m_b) are read
+ *                         (q only when o is non-NULL)
+ *  m            host [B]: matched prefix length, 0 <= m_b <= N_b
+ *  r_num/r_den  the replay ratio r = r_num / r_den, 0 <= r_num <= r_den, r_den > 0;
+ *               k_b = ceil(r m_b) is computed exactly in integers
+ *  S_a          device [B, H, d_v, d_k] or NULL: the exact state at a_b.  When
+ *               given, the same tokens are also run from S_a ("exact twin"),
+ *               giving S_m, so that E_m = S_m - S_hat_m can be formed
+ *  S_hat        device [B, H, d_v, d_k]: the replayed state (zeros when k_b = 0)
+ *  S_exact      device [B, H, d_v, d_k]: required iff S_a is given
+ *  o            device [T, H, d_v] out_dtype or NULL: readout of S_hat over the
+ *               replayed tokens, written at their own stream rows
+ *  a_out, k_out host [B] out (nullable): a_b and k_b
+ */
+gdn_status gdn_tail_replay(const gdn_problem* p, const void* q, const void* k, const void* v,
+                           const float* alpha, const float* beta, const int64_t* m, int32_t r_num,
+                           int32_t r_den, const float* S_a, float* S_hat, float* S_exact, void* o,
+                           int64_t* a_out, int64_t* k_out, void* workspace, size_t ws_bytes,
+                           gdn_stream_t stream);
+
+/* --- host-only helpers (no GPU needed) ------------------------------------------------ */
+
+/* Tail-Replay notes page, section 2.1 table: k = ceil(r_num * m / r_den), a = m - k.
+ * GDN_ERR_INVALID_ARG when m < 0, m > 2^40, r_den <= 0 or r_num outside [0, r_den]. */
+gdn_status gdn_replay_plan(int64_t m, int32_t r_num, int32_t r_den, int64_t* a, int64_t* k);
+
+/* "Sparse prefix caching ...", section 3: *j = 0-based index of the deepest
+ * c_i <= d in the strictly increasing c[0..M), or -1 when none (resume from
+ * the initial state).  GDN_ERR_INVALID_ARG when c is not strictly increasing. */
+gdn_status gdn_select_ckpt(const int64_t* c, int32_t M, int64_t d, int32_t* j);
+
+/* Bytes of workspace every device entry point needs. */
+size_t gdn_workspace_size(void);
+
+/* Zero the sticky status word of a workspace (enqueued on stream). */
+gdn_status gdn_clear_status(void* workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/* Synchronise `stream` and report the workspace's sticky device status:
+ * GDN_OK, or GDN_ERR_DEVICE_TIMEOUT if any kernel that used it gave up on a wait. */
+gdn_status gdn_read_status(const void* workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/* Time limit, in nanoseconds, of every device-side wait of later launches
+ * from this process (default 2 s; 0 restores the default). */
+void gdn_set_wait_limit_ns(uint64_t ns);
+
+/* Human-readable name of a status code. */
+const char* gdn_status_string(gdn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_SCAN_H */
