@@ -157,6 +157,37 @@ gdn_status gdn_tail_replay(const gdn_problem* p, const void* q, const void* k, c
                            int64_t* a_out, int64_t* k_out, void* workspace, size_t ws_bytes,
                            gdn_stream_t stream);
 
+/*
+ * Prefill with sparse checkpoints for callers that cannot allocate device memory.
+ * (No counterpart on the pages: this is a calling convention of this library.)
+ *
+ * Same arguments and results as gdn_prefill_ckpt, without the workspace. It is
+ * meant for callers that are handed their input and output buffers but have
+ * no device allocator of their own -- for instance a plugin inside a serving
+ * engine whose memory pool owns all of HBM, or a latency-critical loop that
+ * cannot afford cudaMalloc's implicit synchronisation. Neither this call nor
+ * anything it calls allocates device memory.
+ *
+ * Instead of a workspace it uses a 256-byte static device array inside the
+ * library (the maximum scratch it can hold; a build whose scan needs more
+ * returns GDN_ERR_UNSUPPORTED). Every GPU that loads the library keeps that
+ * array until the process exits.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array. The call clears it on
+ *    `stream` before launching, so calls whose work overlaps on the GPU (e.g.
+ *    from several host threads on different streams) race on it; serialise them.
+ *  - The call synchronises `stream` before returning, so that it can report a
+ *    device-side wait expiry (GDN_ERR_DEVICE_TIMEOUT) without a workspace.
+ *  - Invalid arguments are rejected exactly as by gdn_prefill_ckpt; only the
+ *    library's own array has been cleared by then.
+ */
+gdn_status gdn_prefill_ckpt_noalloc(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                    const float* alpha, const float* beta, const float* S0, void* o,
+                                    float* S_final, const int64_t* ckpt_pos, const int64_t* cu_ckpt,
+                                    float* ckpt_states, gdn_stream_t stream);
+
 /* --- host-only helpers (no GPU needed) ------------------------------------------------ */
 
 /* Tail-Replay notes page, section 2.1 table: k = ceil(r_num * m / r_den), a = m - k.
