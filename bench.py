@@ -48,8 +48,23 @@ FP32_LANES_PER_SM = 128
 SM_COUNT = 152
 SM_MAX_MHZ = 2070.0
 PEAK_ALU_TFLOPS = SM_COUNT * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12  # 80.54
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_scan_prefill_8x16x8192.md")
-KERNEL_SRC = os.path.join(ROOT, "hybrid_model_recurrent_gb300", "csrc", "gdn_kernel.cuh")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_prefill_8x16x8192.md")
+KERNEL_SRC = os.path.join(ROOT, "hybrid_model_recurrent_gb300", "csrc", "gdn_chunk.cuh")
+# mma.sync m16n8k16 instructions per warp per 64-token chunk in the chunked kernel (8 warps,
+# 2048 MAC each): K K^T / Q K^T 64, blocked substitution 152, U and Q S_0^T 320, P U 96, update 128
+CHUNK_MMA_PER_WARP = 760
+
+
+def measured_peaks():
+    """(hbm GB/s, bf16 TFLOP/s burst, source) from MEASURED_PEAKS.json, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 # -------------------------------------------------------------------------------------------
@@ -380,7 +395,16 @@ def run_ours(args, ws, rank, local):
     _, _, e2e_thr = aggregate(step.units() * e2e_steps, e2e_el, ws, dev)
 
     flops_per_launch = 3 * w.dv * w.dk * 2 * w.T * w.H   # 3 FMAs per state element per tok*head
-    achieved = flops_per_launch / (prefill_ms * 1e-3) / 1e12
+    # algorithmic bytes per tok*head: q, k, v (bf16) + alpha, beta (fp32) + o (bf16)
+    # + the checkpoint and final states amortised over the sequence
+    es = 2
+    n_ck = len(step.ck[0])
+    bytes_tok_head = (2 * w.dk + w.dv) * es + 8 + w.dv * es + (n_ck + 1) * w.dv * w.dk * 4 / w.seq_lens[0]
+    bytes_per_launch = bytes_tok_head * w.T * w.H
+    achieved_gbs = bytes_per_launch / (prefill_ms * 1e-3) / 1e9
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    chunks = w.B * w.H * ((w.seq_lens[0] + 63) // 64)
+    mma_flops = chunks * 8 * CHUNK_MMA_PER_WARP * 2048 * 2
     base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
     if rank == 0:
         line = {
@@ -391,11 +415,20 @@ def run_ours(args, ws, rank, local):
             "e2e": {"value": e2e_thr / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
             "gpu_launches": step.launches_per_step * args.steps,
-            "roofline": {"bound": "alu", "kernel": "gdn_scan_kernel<128,bf16,bf16,readout> (prefill)",
-                         "achieved": achieved, "peak": PEAK_ALU_TFLOPS, "unit": "TFLOP/s",
-                         "frac": achieved / PEAK_ALU_TFLOPS, "traffic": profile_traffic(),
-                         "launch_ms": prefill_ms, "algorithmic_flops_per_launch": flops_per_launch,
-                         "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz (derived, not measured)"},
+            "roofline": {"bound": "hbm", "kernel": "gdn_chunk_kernel<bf16 out, readout> (prefill)",
+                         "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved_gbs / hbm_peak, "traffic": profile_traffic(),
+                         "launch_ms": prefill_ms, "algorithmic_bytes_per_launch": bytes_per_launch,
+                         "algorithmic_bytes_per_tok_head": bytes_tok_head,
+                         "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_src})",
+                         "tensor_view": {"executed_mma_tflops": mma_flops / (prefill_ms * 1e-3) / 1e12,
+                                         "peak_bf16_tflops": bf16_peak,
+                                         "frac": mma_flops / (prefill_ms * 1e-3) / 1e12 / bf16_peak},
+                         "fp32_alu_equivalent": {
+                             "algorithmic_tflops": flops_per_launch / (prefill_ms * 1e-3) / 1e12,
+                             "peak_tflops": PEAK_ALU_TFLOPS,
+                             "frac": flops_per_launch / (prefill_ms * 1e-3) / 1e12 / PEAK_ALU_TFLOPS,
+                             "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"}},
             "phases": {k: v for k, v in step.tok_head.items()},
             "states_per_s": sum(len(c) for c in step.ck) * w.H * args.steps / slowest,
             "cpu_baseline": base,

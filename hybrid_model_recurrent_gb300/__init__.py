@@ -28,6 +28,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn_scan.so")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = range(5)
 GDN_F32, GDN_BF16 = 0, 1
+ALGO = {"auto": 0, "per_token": 1, "chunked": 2}
 
 _lock = threading.Lock()
 _lib = None
@@ -43,7 +44,7 @@ class GdnError(RuntimeError):
 class _Problem(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("cu_seqlens", ctypes.POINTER(ctypes.c_int64)),
-                ("qkv_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+                ("qkv_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("algo", ctypes.c_int)]
 
 
 def build(force: bool = False) -> str:
@@ -165,8 +166,10 @@ def gdn_select_ckpt(c: Sequence[int], d: int) -> int:
     return j.value
 
 
-def _problem(cu: np.ndarray, H: int, dk: int, dv: int, qkv_dtype: torch.dtype, out_dtype: torch.dtype):
+def _problem(cu: np.ndarray, H: int, dk: int, dv: int, qkv_dtype: torch.dtype, out_dtype: torch.dtype,
+             algo: str = "auto"):
     pr = _Problem()
+    pr.algo = ALGO[algo]
     pr.num_seqs = len(cu) - 1
     pr.num_heads = H
     pr.d_k = dk
@@ -193,7 +196,7 @@ def _flatten_ckpts(ckpt_pos, B: int):
 
 def gdn_prefill_ckpt(q, k, v, alpha, beta, cu_seqlens, *, S0=None, ckpt_pos=None, readout: bool = True,
                      out_dtype: Optional[torch.dtype] = None, o=None, S_final=None, ckpt_states=None,
-                     stream=None, ws: Optional[torch.Tensor] = None):
+                     stream=None, ws: Optional[torch.Tensor] = None, algo: str = "auto"):
     """Prefill with sparse checkpoints.  ckpt_pos: one list of 1-based positions per sequence.
 
     Returns dict(o=[T,H,dv] or None, S_final=[B,H,dv,dk], ckpt_states=[M_total,H,dv,dk])."""
@@ -214,7 +217,7 @@ def gdn_prefill_ckpt(q, k, v, alpha, beta, cu_seqlens, *, S0=None, ckpt_pos=None
     if ckpt_states is None and n_ck > 0:
         ckpt_states = torch.empty((n_ck, H, dv, dk), dtype=torch.float32, device=dev)
     ws = ws if ws is not None else workspace(dev)
-    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_prefill_ckpt(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
                                 _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
                                 _p64(flat) if n_ck > 0 else None, _p64(cu_ck), _ptr(ckpt_states),
@@ -225,7 +228,7 @@ def gdn_prefill_ckpt(q, k, v, alpha, beta, cu_seqlens, *, S0=None, ckpt_pos=None
 
 def gdn_resume_from_ckpt(q, k, v, alpha, beta, cu_seqlens, ckpt_states, ckpt_pos, probes, *, S0=None,
                          readout: bool = True, out_dtype: Optional[torch.dtype] = None, S_out=None, o_out=None,
-                         stream=None, ws: Optional[torch.Tensor] = None):
+                         stream=None, ws: Optional[torch.Tensor] = None, algo: str = "auto"):
     """Resume at the probes' depths.  probes: list of (seq, depth).
 
     Returns dict(S_out=[P,H,dv,dk], o=[R,H,dv] or None, chosen=[P] positions c_j, offsets=[P+1])."""
@@ -255,7 +258,7 @@ def gdn_resume_from_ckpt(q, k, v, alpha, beta, cu_seqlens, ckpt_states, ckpt_pos
     if S_out is None:
         S_out = torch.empty((P, H, dv, dk), dtype=torch.float32, device=dev)
     ws = ws if ws is not None else workspace(dev)
-    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_resume_from_ckpt(
         ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
         _ptr(ckpt_states), _p64(flat) if n_ck > 0 else None, _p64(cu_ck), P,
@@ -268,7 +271,7 @@ def gdn_resume_from_ckpt(q, k, v, alpha, beta, cu_seqlens, ckpt_states, ckpt_pos
 
 def gdn_tail_replay(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int, *, S_a=None, readout: bool = False,
                     out_dtype: Optional[torch.dtype] = None, S_hat=None, S_exact=None, o=None, stream=None,
-                    ws: Optional[torch.Tensor] = None):
+                    ws: Optional[torch.Tensor] = None, algo: str = "auto"):
     """Tail-Replay at matched lengths m (one per sequence).
 
     Returns dict(S_hat, S_exact or None, o or None, a=[B], k=[B])."""
@@ -290,7 +293,7 @@ def gdn_tail_replay(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int,
     a_out = np.zeros(B, dtype=np.int64)
     k_out = np.zeros(B, dtype=np.int64)
     ws = ws if ws is not None else workspace(dev)
-    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_tail_replay(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
                                _ptr(beta), _p64(mm), r_num, r_den, _ptr(S_a), _ptr(S_hat),
                                _ptr(S_exact if S_a is not None else None), _ptr(o), _p64(a_out), _p64(k_out),

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "../../include/gdn_scan.h"
+#include "gdn_chunk.cuh"
 #include "gdn_kernel.cuh"
 
 #define GDN_EXPORT extern "C" __attribute__((visibility("default")))
@@ -44,21 +45,29 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool supported_d(int d) { return d == 32 || d == 64 || d == 128; }
 
-// [T, H, d] stream, box (box_x, 1, kChunk)
-bool make_stream_map(CUtensorMap* m, const void* base, bool bf16, int64_t T, int H, int d, int box_x) {
+// [T, H, d] stream, box (box_x, 1, box_t)
+bool make_stream_map(CUtensorMap* m, const void* base, bool bf16, int64_t T, int H, int d, int box_x,
+                     int box_t = gdn::kChunk, bool swizzle128 = false) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const size_t es = bf16 ? 2 : 4;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)std::max<int64_t>(T, 1)};
     cuuint64_t strides[2] = {(cuuint64_t)(d * es), (cuuint64_t)((size_t)H * d * es)};
-    cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)gdn::kChunk};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)box_t};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+bool chunked_ok(const gdn_problem* p) {
+    return p->d_k == gdn::chunk::D && p->d_v == gdn::chunk::D && p->qkv_dtype == GDN_BF16;
+}
+
+bool use_chunked(const gdn_problem* p) { return p->algo != GDN_ALGO_PER_TOKEN && chunked_ok(p); }
 
 // Common validation of the problem description; fills seq lengths.
 gdn_status check_problem(const gdn_problem* p, std::vector<int64_t>& lens) {
@@ -66,7 +75,10 @@ gdn_status check_problem(const gdn_problem* p, std::vector<int64_t>& lens) {
     if (p->num_seqs < 1 || p->num_heads < 1 || p->d_k < 1 || p->d_v < 1) return GDN_ERR_INVALID_ARG;
     if ((p->qkv_dtype != GDN_F32 && p->qkv_dtype != GDN_BF16) || (p->out_dtype != GDN_F32 && p->out_dtype != GDN_BF16))
         return GDN_ERR_INVALID_ARG;
+    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_PER_TOKEN && p->algo != GDN_ALGO_CHUNKED)
+        return GDN_ERR_INVALID_ARG;
     if (!supported_d(p->d_k) || !supported_d(p->d_v)) return GDN_ERR_UNSUPPORTED;
+    if (p->algo == GDN_ALGO_CHUNKED && !chunked_ok(p)) return GDN_ERR_UNSUPPORTED;
     if (p->cu_seqlens[0] != 0) return GDN_ERR_INVALID_ARG;
     lens.resize(p->num_seqs);
     for (int b = 0; b < p->num_seqs; ++b) {
@@ -124,13 +136,85 @@ struct LaunchSpec {
     bool twin;
 };
 
+// Batch jobs into parameter blocks and launch each with `launch(params, n_jobs)`.
+template <class F>
+gdn_status launch_batches(gdn::Params& prm, std::vector<HostJob>& jobs, F&& launch) {
+    size_t i = 0;
+    while (i < jobs.size()) {
+        int nj = 0, nc = 0;
+        while (i + nj < jobs.size() && nj < gdn::kMaxJobs &&
+               nc + (int)jobs[i + nj].ckpts.size() <= gdn::kMaxCkpts) {
+            gdn::Job j = jobs[i + nj].job;
+            j.ck_begin = nc;
+            j.ck_count = (int32_t)jobs[i + nj].ckpts.size();
+            for (const gdn::Ckpt& c : jobs[i + nj].ckpts) prm.ckpts[nc++] = c;
+            prm.jobs[nj++] = j;
+        }
+        if (nj == 0) return GDN_ERR_UNSUPPORTED;  // one job with more checkpoints than a launch holds
+        prm.n_jobs = nj;
+        if (launch(prm, nj) != cudaSuccess) return GDN_ERR_CUDA;
+        i += nj;
+    }
+    return GDN_OK;
+}
+
+// Chunked tensor-core path (d_k = d_v = 128, bf16): one CTA per (job, head).
+gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_t stream) {
+    const gdn_problem* p = L.p;
+    const int H = p->num_heads;
+    if ((int64_t)H * gdn::kMaxJobs > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    // the exact twin runs as a second job over the same tokens from S_a
+    if (L.twin) {
+        const size_t n = jobs.size();
+        for (size_t i = 0; i < n; ++i) {
+            HostJob t = jobs[i];
+            t.job.s0 = jobs[i].job.s0_twin;
+            t.job.s_final = jobs[i].job.s_final_twin;
+            t.job.o_row_begin = -1;
+            t.job.s0_twin = nullptr;
+            t.job.s_final_twin = nullptr;
+            jobs.push_back(t);
+        }
+    }
+    std::stable_sort(jobs.begin(), jobs.end(),
+                     [](const HostJob& a, const HostJob& b) { return a.job.len > b.job.len; });
+    const int64_t T = p->cu_seqlens[p->num_seqs];
+    auto prm = std::make_unique<gdn::Params>();
+    std::memset(prm.get(), 0, sizeof(gdn::Params));
+    const int D = gdn::chunk::D, C = gdn::chunk::C;
+    bool maps = true;
+    if (L.k) maps = maps && make_stream_map(&prm->tm_k, L.k, true, T, H, D, 64, C, true);
+    if (L.q) maps = maps && make_stream_map(&prm->tm_q, L.q, true, T, H, D, 64, C, true);
+    if (L.v) maps = maps && make_stream_map(&prm->tm_v, L.v, true, T, H, D, 64, C, true);
+    if (!maps) return GDN_ERR_CUDA;
+    // without a readout the q tiles are still staged: point them at k
+    if (!L.q && L.k) prm->tm_q = prm->tm_k;
+    prm->alpha = L.alpha;
+    prm->beta = L.beta;
+    prm->o = L.o;
+    prm->ckpt_states = L.ckpt_states;
+    prm->status = L.status;
+    prm->wait_limit_ns = g_wait_ns.load();
+    prm->H = H;
+    prm->dv = D;
+    const bool out_bf16 = p->out_dtype == GDN_BF16;
+    return launch_batches(*prm, jobs, [&](const gdn::Params& pr, int nj) -> cudaError_t {
+        const int grid = nj * H;
+        if (L.readout)
+            return out_bf16 ? gdn::chunk::launch_chunk<true, true>(pr, grid, stream)
+                            : gdn::chunk::launch_chunk<false, true>(pr, grid, stream);
+        return gdn::chunk::launch_chunk<false, false>(pr, grid, stream);
+    });
+}
+
 // Sort jobs longest first and launch them in batches that fit one parameter block.
 gdn_status run_jobs(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_t stream) {
     const gdn_problem* p = L.p;
+    if (use_chunked(p)) return run_jobs_chunked(L, jobs, stream);
     const int H = p->num_heads, dv = p->d_v, dk = p->d_k;
     const bool in_bf16 = p->qkv_dtype == GDN_BF16;
     const bool out_bf16 = p->out_dtype == GDN_BF16;
-    const int wr = L.twin ? 16 : 32;               // real rows per consumer warp
+    const int wr = gdn::kSlotsPerWarp / (L.twin ? 2 : 1);   // real rows per consumer warp
     const int nw = std::min(gdn::kMaxConsumerWarps, dv / wr);
     const int rows = nw * wr;
     const int ctas_per_head = dv / rows;
@@ -174,25 +258,9 @@ gdn_status run_jobs(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_
     if (!fn) return GDN_ERR_UNSUPPORTED;
     const size_t smem = gdn::smem_bytes(dk, in_bf16 ? 2 : 4, rows, L.readout);
 
-    size_t i = 0;
-    while (i < jobs.size()) {
-        int nj = 0, nc = 0;
-        while (i + nj < jobs.size() && nj < gdn::kMaxJobs &&
-               nc + (int)jobs[i + nj].ckpts.size() <= gdn::kMaxCkpts) {
-            gdn::Job j = jobs[i + nj].job;
-            j.ck_begin = nc;
-            j.ck_count = (int32_t)jobs[i + nj].ckpts.size();
-            for (const gdn::Ckpt& c : jobs[i + nj].ckpts) prm->ckpts[nc++] = c;
-            prm->jobs[nj++] = j;
-        }
-        if (nj == 0) return GDN_ERR_UNSUPPORTED;  // one job with more checkpoints than a launch holds
-        prm->n_jobs = nj;
-        const int grid = nj * H * ctas_per_head;
-        cudaError_t e = fn(*prm, grid, smem, stream);
-        if (e != cudaSuccess) return GDN_ERR_CUDA;
-        i += nj;
-    }
-    return GDN_OK;
+    return launch_batches(*prm, jobs, [&](const gdn::Params& pr, int nj) -> cudaError_t {
+        return fn(pr, nj * H * ctas_per_head, smem, stream);
+    });
 }
 
 }  // namespace

@@ -10,10 +10,12 @@
 // Design (one CTA = one (job, head, block of state rows)):
 //  * Row i of S evolves only from v_{t,i}: the key-space operator acts from the
 //    right, so the rows of a head split across lanes, warps and CTAs with no
-//    exchange.  Each consumer warp owns 32 state rows ("slots"); a lane holds an
-//    R x C register tile (R = C-lanes per row group, R*C = d_k), so the dot
-//    products S k and S q reduce over NCL lanes with a reduce-scatter that leaves
-//    lane `cl` holding the full sums of slot `cl`.
+//    exchange.  A consumer warp owns 16 state rows ("slots"): lanes form 4 row
+//    groups of 8 column lanes, and a lane holds a 4-row x (d_k/8)-column register
+//    tile.  The dot products S k and S q reduce over the 8 column lanes with a
+//    reduce-scatter that leaves lanes 2s and 2s+1 of a group with slot s's sums.
+//    Two or more consumer warps share each SM sub-partition, hiding each other's
+//    per-token dependency chain.
 //  * The state is kept in a running scale: S = s * St.  With s_t = alpha_t s_{t-1}
 //    the update becomes St += c k^T with c = (beta/s_t) v - beta (St_{t-1} k), so
 //    each state element costs exactly three FMAs per token (update, S k, S q),
@@ -22,10 +24,11 @@
 //    (St *= s, s = 1) whenever the scale would fall below 2^-32, at every
 //    checkpoint and after the last token, so dumps and results are plain states
 //    and the arithmetic after a checkpoint does not depend on the path before it.
-//  * One producer warp stages k, q, v tiles of 32 tokens with TMA into a 4-deep
-//    shared-memory ring guarded by mbarriers; consumers widen bf16 to fp32 on
-//    load.  Every wait is bounded by a wall-clock limit; on expiry the kernel
-//    records GDN device status and returns (never hangs).
+//  * One producer warp stages k, q, v tiles of 32 tokens with TMA into a 3-deep
+//    shared-memory ring guarded by mbarriers, widens bf16 k and q to fp32 once
+//    per CTA (consumers then read fp32 with conflict-free broadcast loads) and
+//    publishes the per-token scalars.  Every wait is bounded by a wall-clock
+//    limit; on expiry the kernel records the device status and returns.
 #pragma once
 
 #include <cuda.h>
@@ -38,10 +41,11 @@
 namespace gdn {
 
 constexpr int kChunk = 32;     // tokens per pipeline stage
-constexpr int kStages = 4;     // depth of the shared-memory ring
+constexpr int kStages = 3;     // depth of the shared-memory ring
 constexpr int kMaxJobs = 256;  // jobs per launch (host splits larger batches)
 constexpr int kMaxCkpts = 1536;
-constexpr int kMaxConsumerWarps = 4;
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kSlotsPerWarp = 16;   // state rows (slots) held by one consumer warp
 constexpr float kRenormFloor = 0x1p-32f;
 
 enum : uint32_t { FLAG_RENORM = 1u, FLAG_DUMP = 2u, FLAG_INDEX_SHIFT = 8u };
@@ -100,6 +104,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+        "r"(bytes)
+        : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
@@ -147,43 +157,63 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Reduce-scatter over the NCL lanes of a row group: on entry v[i] is this lane's
-// partial sum for slot i; on exit the return value is the full sum of slot
-// (lane & (NCL-1)).
-template <int RT>
-__device__ __forceinline__ float reduce_scatter(float (&v)[RT], int lane) {
+// Reduce over the 8 column lanes of a row group.  On entry v[i] is this lane's
+// partial sum for slot i (4 slots); on exit the return value is the full sum of
+// slot (cl >> 1) & 3, held by lanes cl = 2s and 2s+1 of the group.
+__device__ __forceinline__ float reduce_slots(float (&v)[4], int lane) {
+    {
+        const bool up = (lane & 4) != 0;
 #pragma unroll
-    for (int half = RT / 2; half >= 1; half >>= 1) {
-        const bool up = (lane & half) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = up ? v[i] : v[i + half];
-            const float keep = up ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        for (int i = 0; i < 2; ++i) {
+            const float send = up ? v[i] : v[i + 2];
+            const float keep = up ? v[i + 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
         }
     }
-    return v[0];
+    {
+        const bool up = (lane & 2) != 0;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 // Shared-memory layout of one pipeline stage.
+//   kf, qf : [kChunk][dk] fp32, read by the consumers
+//   v      : [kChunk][rows] input dtype
+//   sc     : [kChunk] float4 {s_t, beta_t / s_t, beta_t, flags}
+//   kr, qr : [kChunk][dk] bf16 TMA landing buffers (bf16 inputs only)
 struct StageLayout {
-    uint32_t k_off, q_off, v_off, sc_off, bytes, tx_bytes;
+    uint32_t kf_off, qf_off, v_off, sc_off, kr_off, qr_off, bytes, tx_bytes;
 };
 __host__ __device__ constexpr uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
 __host__ __device__ inline StageLayout stage_layout(int dk, int in_bytes, int rows, bool readout) {
     StageLayout L{};
-    const uint32_t kb = (uint32_t)(kChunk * dk * in_bytes);
+    const uint32_t kf = (uint32_t)(kChunk * dk * 4);
+    const uint32_t kr = (uint32_t)(kChunk * dk * in_bytes);
     const uint32_t vb = (uint32_t)(kChunk * rows * in_bytes);
-    L.k_off = 0;
-    L.q_off = align128(kb);
-    L.v_off = L.q_off + (readout ? align128(kb) : 0u);
-    L.sc_off = L.v_off + align128(vb);
-    L.bytes = align128(L.sc_off + kChunk * 16u);
-    L.tx_bytes = kb * (readout ? 2u : 1u) + vb;
+    const bool raw = in_bytes != 4;
+    uint32_t off = 0;
+    L.kf_off = off;
+    off += align128(kf);
+    L.qf_off = off;
+    if (readout) off += align128(kf);
+    L.v_off = off;
+    off += align128(vb);
+    L.sc_off = off;
+    off += align128(kChunk * 16u);
+    L.kr_off = off;
+    if (raw) off += align128(kr);
+    L.qr_off = off;
+    if (raw && readout) off += align128(kr);
+    L.bytes = align128(off);
+    L.tx_bytes = kr * (readout ? 2u : 1u) + vb;
     return L;
 }
+// barriers: raw[kStages], full[kStages], empty[kStages]
 __host__ __device__ inline uint32_t smem_bytes(int dk, int in_bytes, int rows, bool readout) {
-    return stage_layout(dk, in_bytes, rows, readout).bytes * kStages + 2u * kStages * 8u + 128u;
+    return stage_layout(dk, in_bytes, rows, readout).bytes * kStages + 3u * kStages * 8u + 128u;
 }
 
 // ------------------------------------------------------------------------------------
@@ -193,16 +223,16 @@ template <int DK, bool IN_BF16, bool OUT_BF16, bool READOUT, bool TWIN>
 __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     gdn_scan_kernel(const __grid_constant__ Params p) {
     constexpr int ES = IN_BF16 ? 2 : 4;
-    constexpr int NCL = DK >= 64 ? 8 : 4;    // lanes sharing one row group
-    constexpr int RT = NCL;                  // row slots per lane
-    constexpr int CT = DK / NCL;             // columns per lane
+    constexpr int NCL = 8;                   // column lanes per row group
+    constexpr int RT = 4;                    // row slots per lane
+    constexpr int CT = DK / NCL;             // columns per lane (16, 8, 4)
     constexpr int CT2 = CT / 2;
-    constexpr int CH = 16 / ES;              // elements per 16-byte chunk
-    constexpr int NCH = CT / CH;             // chunks per lane per row
+    constexpr int CH4 = CT / 4;              // fp32 float4 chunks per lane and vector
     constexpr int NRG = 32 / NCL;            // row groups per warp
     constexpr int HALF = TWIN ? RT / 2 : RT; // real rows per lane per state
-    constexpr int WR = NRG * HALF;           // real rows per warp
-    static_assert(NCH >= 1 && CT % CH == 0 && CT % 2 == 0, "lane tile");
+    constexpr int WR = NRG * HALF;           // real rows per warp (16, or 8 with the twin)
+    static_assert(CH4 >= 1 && CT % 4 == 0, "lane tile");
+    static_assert(NRG * RT == kSlotsPerWarp, "slots per warp");
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
 
     extern __shared__ unsigned char smem_raw[];
@@ -214,7 +244,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const StageLayout L = stage_layout(DK, ES, RB, READOUT);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bytes * kStages);
+    uint64_t* rawb = reinterpret_cast<uint64_t*>(smem + L.bytes * kStages);
+    uint64_t* full = rawb + kStages;
     uint64_t* empty = full + kStages;
 
     const int per_job = p.H * p.ctas_per_head;
@@ -231,6 +262,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
+            mbar_init(&rawb[s], 1);
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], (uint32_t)nw);
         }
@@ -253,12 +285,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
                 break;
             }
             unsigned char* stage = smem + (size_t)st * L.bytes;
+            uint64_t* landing = IN_BF16 ? &rawb[st] : &full[st];
             if (lane == 0) {
-                mbar_expect_tx(&full[st], L.tx_bytes);
+                // bf16: the landing barrier completes on the copies alone (one arrival
+                // here); fp32: the copies land on `full`, which the producer arrives
+                // on after publishing the scalars
+                if constexpr (IN_BF16)
+                    mbar_arrive_expect_tx(landing, L.tx_bytes);
+                else
+                    mbar_expect_tx(landing, L.tx_bytes);
                 const int t0 = (int)(tok_begin + (int64_t)c * kChunk);
-                tma_load_3d(stage + L.k_off, &p.tm_k, 0, h, t0, &full[st]);
-                if (READOUT) tma_load_3d(stage + L.q_off, &p.tm_q, 0, h, t0, &full[st]);
-                tma_load_3d(stage + L.v_off, &p.tm_v, rb * RB, h, t0, &full[st]);
+                tma_load_3d(stage + (IN_BF16 ? L.kr_off : L.kf_off), &p.tm_k, 0, h, t0, landing);
+                if (READOUT) tma_load_3d(stage + (IN_BF16 ? L.qr_off : L.qf_off), &p.tm_q, 0, h, t0, landing);
+                tma_load_3d(stage + L.v_off, &p.tm_v, rb * RB, h, t0, landing);
             }
             issued = c + 1;
             const int base = c * kChunk;
@@ -299,12 +338,31 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             s_carry = s;
             const float b1 = __fdiv_rn(b, my_s);
             reinterpret_cast<float4*>(stage + L.sc_off)[lane] = make_float4(my_s, b1, b, __uint_as_float(my_fl));
+            if constexpr (IN_BF16) {
+                // widen k (and q) to fp32 once for all consumer warps
+                if (!warp_wait(&rawb[st], (uint32_t)((c / kStages) & 1), limit)) {
+                    ok = false;
+                    break;   // this chunk's copy stays accounted for by the drain below
+                }
+                constexpr int NV4 = kChunk * DK / 4;   // groups of 4 elements
+#pragma unroll 4
+                for (int g = lane; g < NV4; g += 32) {
+                    const uint2 w = reinterpret_cast<const uint2*>(stage + L.kr_off)[g];
+                    const float2 lo = bf16x2_to_float2(w.x), hi = bf16x2_to_float2(w.y);
+                    reinterpret_cast<float4*>(stage + L.kf_off)[g] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    if (READOUT) {
+                        const uint2 u = reinterpret_cast<const uint2*>(stage + L.qr_off)[g];
+                        const float2 ql = bf16x2_to_float2(u.x), qh = bf16x2_to_float2(u.y);
+                        reinterpret_cast<float4*>(stage + L.qf_off)[g] = make_float4(ql.x, ql.y, qh.x, qh.y);
+                    }
+                }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[st]);
         }
         // never leave with copies in flight into this CTA's shared memory
         for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
-            warp_wait(&full[c % kStages], (uint32_t)((c / kStages) & 1), limit);
+            warp_wait(IN_BF16 ? &rawb[c % kStages] : &full[c % kStages], (uint32_t)((c / kStages) & 1), limit);
         if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
         return;
     }
@@ -312,46 +370,36 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     // ================================ consumer warps ===============================
     const int cl = lane & (NCL - 1);
     const int rg = lane / NCL;
-    const int my_state = TWIN ? (cl / HALF) : 0;
-    const int my_row = warp * WR + rg * HALF + (TWIN ? (cl % HALF) : cl);  // CTA-relative real row
-    const int grow_base = rb * RB + warp * WR + rg * HALF;                  // head row of slot 0
+    const int my_slot = (cl >> 1) & 3;                                   // slot whose sums this lane holds
+    const int my_state = TWIN ? (my_slot / HALF) : 0;
+    const int row0 = warp * WR + rg * HALF;                              // CTA row of this group's slot 0
+    const int my_row = row0 + (TWIN ? (my_slot % HALF) : my_slot);       // CTA-relative real row
+    const int grow_base = rb * RB + row0;                                // head row of slot 0
     const size_t head_state = (size_t)h * (size_t)dv * DK;
 
+    // state tile: S[i][2*j4 + e] holds columns 4*(cl + 8*j4) + 2*e .. +1 of slot i
     float2 S[RT][CT2];
-    {
 #pragma unroll
-        for (int i = 0; i < RT; ++i) {
-            const int state = TWIN ? (i / HALF) : 0;
-            const int grow = grow_base + (TWIN ? (i % HALF) : i);
-            const float* src = state == 0 ? p.jobs[job_idx].s0 : p.jobs[job_idx].s0_twin;
+    for (int i = 0; i < RT; ++i) {
+        const int state = TWIN ? (i / HALF) : 0;
+        const int grow = grow_base + (TWIN ? (i % HALF) : i);
+        const float* src = state == 0 ? p.jobs[job_idx].s0 : p.jobs[job_idx].s0_twin;
 #pragma unroll
-            for (int jc = 0; jc < NCH; ++jc) {
-                const int col0 = (cl + NCL * jc) * CH;
-#pragma unroll
-                for (int e4 = 0; e4 < CH / 4; ++e4) {
-                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (src) x = __ldg(reinterpret_cast<const float4*>(src + head_state + (size_t)grow * DK + col0) + e4);
-                    S[i][jc * (CH / 2) + e4 * 2 + 0] = make_float2(x.x, x.y);
-                    S[i][jc * (CH / 2) + e4 * 2 + 1] = make_float2(x.z, x.w);
-                }
-            }
+        for (int j4 = 0; j4 < CH4; ++j4) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (src) x = __ldg(reinterpret_cast<const float4*>(src + head_state + (size_t)grow * DK) + cl + NCL * j4);
+            S[i][2 * j4 + 0] = make_float2(x.x, x.y);
+            S[i][2 * j4 + 1] = make_float2(x.z, x.w);
         }
     }
 
     auto load_vec = [&](const unsigned char* tok, float2 (&dst)[CT2]) {
-        const uint4* p4 = reinterpret_cast<const uint4*>(tok);
+        const float4* p4 = reinterpret_cast<const float4*>(tok);
 #pragma unroll
-        for (int jc = 0; jc < NCH; ++jc) {
-            const uint4 w = p4[cl + NCL * jc];
-            if constexpr (IN_BF16) {
-                dst[jc * 4 + 0] = bf16x2_to_float2(w.x);
-                dst[jc * 4 + 1] = bf16x2_to_float2(w.y);
-                dst[jc * 4 + 2] = bf16x2_to_float2(w.z);
-                dst[jc * 4 + 3] = bf16x2_to_float2(w.w);
-            } else {
-                dst[jc * 2 + 0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
-                dst[jc * 2 + 1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
-            }
+        for (int j4 = 0; j4 < CH4; ++j4) {
+            const float4 w = p4[cl + NCL * j4];
+            dst[2 * j4 + 0] = make_float2(w.x, w.y);
+            dst[2 * j4 + 1] = make_float2(w.z, w.w);
         }
     };
     auto load_v = [&](const unsigned char* stage, int tau) -> float {
@@ -361,24 +409,41 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         else
             return *reinterpret_cast<const float*>(pv);
     };
-    auto dot_k = [&](const float2 (&kv)[CT2], float (&out)[RT]) {
+    auto dot_slots = [&](const float2 (&x)[CT2], float (&out)[RT]) {
+        float2 acc[RT];
 #pragma unroll
-        for (int i = 0; i < RT; ++i) {
-            float2 acc = make_float2(0.f, 0.f);
+        for (int i = 0; i < RT; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int jj = 0; jj < CT2; ++jj) acc = __ffma2_rn(S[i][jj], kv[jj], acc);
-            out[i] = acc.x + acc.y;
-        }
+        for (int jj = 0; jj < CT2; ++jj)
+#pragma unroll
+            for (int i = 0; i < RT; ++i) acc[i] = __ffma2_rn(S[i][jj], x[jj], acc[i]);
+#pragma unroll
+        for (int i = 0; i < RT; ++i) out[i] = acc[i].x + acc[i].y;
     };
     auto broadcast_c = [&](float c_mine, float (&creg)[RT]) {
         const int grp = lane & ~(NCL - 1);
 #pragma unroll
-        for (int i = 0; i < RT; ++i) creg[i] = __shfl_sync(0xffffffffu, c_mine, grp | i);
+        for (int i = 0; i < RT; ++i) creg[i] = __shfl_sync(0xffffffffu, c_mine, grp | (i << 1));
+    };
+    // write the slots of one state (0: the scan, 1: the twin) to dst_head [dv, dk]
+    auto store_state = [&](float* dst_head, int which) {
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            if ((TWIN ? (i / HALF) : 0) != which) continue;
+            const int grow = grow_base + (TWIN ? (i % HALF) : i);
+#pragma unroll
+            for (int j4 = 0; j4 < CH4; ++j4) {
+                const float2 a0 = S[i][2 * j4 + 0], a1 = S[i][2 * j4 + 1];
+                reinterpret_cast<float4*>(dst_head + (size_t)grow * DK)[cl + NCL * j4] =
+                    make_float4(a0.x, a0.y, a1.x, a1.y);
+            }
+        }
     };
 
     bool ok = true;
     float creg[RT];
     float2 kc[CT2];
+    float4 sct = make_float4(1.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RT; ++i) creg[i] = 0.f;
 #pragma unroll
@@ -387,17 +452,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     if (len > 0) {
         ok = warp_wait(&full[0], 0u, limit);
         if (ok) {
-            load_vec(smem + L.k_off, kc);
+            load_vec(smem + L.kf_off, kc);
             float pk[RT];
-            dot_k(kc, pk);
-            const float pkr = reduce_scatter<RT>(pk, lane);
-            const float4 sc = reinterpret_cast<const float4*>(smem + L.sc_off)[0];
+            dot_slots(kc, pk);
+            const float pkr = reduce_slots(pk, lane);
+            sct = reinterpret_cast<const float4*>(smem + L.sc_off)[0];
             const float vv = load_v(smem, 0);
-            broadcast_c(sc.y * vv - sc.z * pkr, creg);
+            broadcast_c(sct.y * vv - sct.z * pkr, creg);
         }
     }
 
     const int64_t o_row0 = p.jobs[job_idx].o_row_begin;
+    OutT* const o_base = reinterpret_cast<OutT*>(p.o) + (size_t)h * (size_t)dv + (size_t)(rb * RB + my_row);
+    const bool o_lane = READOUT && o_row0 >= 0 && my_state == 0 && (cl & 1) == 0;
     for (int tg = 0; ok && tg < len; ++tg) {
         const int c = tg / kChunk;
         const int tau = tg - c * kChunk;
@@ -416,37 +483,48 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
         float2 kn[CT2];
         if (has_next) {
-            load_vec(stage_n + L.k_off + (size_t)taun * DK * ES, kn);
+            load_vec(stage_n + L.kf_off + (size_t)taun * DK * 4, kn);
         } else {
 #pragma unroll
             for (int jj = 0; jj < CT2; ++jj) kn[jj] = make_float2(0.f, 0.f);
         }
         // pass A: St += c k_t^T, then the next token's St k_{t+1}
         float pk[RT];
+        {
+            float2 acc[RT];
+            float2 cc[RT];
 #pragma unroll
-        for (int i = 0; i < RT; ++i) {
-            const float2 cc = make_float2(creg[i], creg[i]);
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int jj = 0; jj < CT2; ++jj) {
-                S[i][jj] = __ffma2_rn(cc, kc[jj], S[i][jj]);
-                acc = __ffma2_rn(S[i][jj], kn[jj], acc);
+            for (int i = 0; i < RT; ++i) {
+                acc[i] = make_float2(0.f, 0.f);
+                cc[i] = make_float2(creg[i], creg[i]);
             }
-            pk[i] = acc.x + acc.y;
+#pragma unroll
+            for (int jj = 0; jj < CT2; ++jj)
+#pragma unroll
+                for (int i = 0; i < RT; ++i) {
+                    S[i][jj] = __ffma2_rn(cc[i], kc[jj], S[i][jj]);
+                    acc[i] = __ffma2_rn(S[i][jj], kn[jj], acc[i]);
+                }
+#pragma unroll
+            for (int i = 0; i < RT; ++i) pk[i] = acc[i].x + acc[i].y;
         }
-        float pkr = reduce_scatter<RT>(pk, lane);
-        const float4 sct = reinterpret_cast<const float4*>(stage + L.sc_off)[tau];
+        float pkr = reduce_slots(pk, lane);
+        float4 scn = make_float4(1.f, 0.f, 0.f, 0.f);
+        float vv = 0.f;
+        if (has_next) {
+            scn = reinterpret_cast<const float4*>(stage_n + L.sc_off)[taun];
+            vv = load_v(stage_n, taun);
+        }
         if constexpr (READOUT) {
             // pass B: readout St q_t of the post-update state
             float2 qv[CT2];
-            load_vec(stage + L.q_off + (size_t)tau * DK * ES, qv);
+            load_vec(stage + L.qf_off + (size_t)tau * DK * 4, qv);
             float pq[RT];
-            dot_k(qv, pq);
-            const float pqr = reduce_scatter<RT>(pq, lane);
-            if (o_row0 >= 0 && my_state == 0) {
+            dot_slots(qv, pq);
+            const float pqr = reduce_slots(pq, lane);
+            if (o_lane) {
                 const float ov = sct.x * pqr;
-                OutT* op = reinterpret_cast<OutT*>(p.o) + ((size_t)(o_row0 + tg) * (size_t)H + (size_t)h) * (size_t)dv +
-                           (size_t)(rb * RB + my_row);
+                OutT* op = o_base + (size_t)(o_row0 + tg) * (size_t)H * (size_t)dv;
                 if constexpr (OUT_BF16)
                     *op = __float2bfloat16_rn(ov);
                 else
@@ -461,36 +539,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
 #pragma unroll
                 for (int jj = 0; jj < CT2; ++jj) S[i][jj] = __fmul2_rn(S[i][jj], ss);
             if (has_next) {
-                dot_k(kn, pk);
-                pkr = reduce_scatter<RT>(pk, lane);
+                dot_slots(kn, pk);
+                pkr = reduce_slots(pk, lane);
             }
             if (fl & FLAG_DUMP) {
                 const int slot = p.ckpts[fl >> FLAG_INDEX_SHIFT].slot;
-                float* dst = p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state;
-#pragma unroll
-                for (int i = 0; i < RT; ++i) {
-                    const int grow = grow_base + (TWIN ? (i % HALF) : i);
-                    if (TWIN && i >= HALF) continue;
-#pragma unroll
-                    for (int jc = 0; jc < NCH; ++jc) {
-                        const int col0 = (cl + NCL * jc) * CH;
-#pragma unroll
-                        for (int e4 = 0; e4 < CH / 4; ++e4) {
-                            const float2 a0 = S[i][jc * (CH / 2) + e4 * 2 + 0];
-                            const float2 a1 = S[i][jc * (CH / 2) + e4 * 2 + 1];
-                            reinterpret_cast<float4*>(dst + (size_t)grow * DK + col0)[e4] =
-                                make_float4(a0.x, a0.y, a1.x, a1.y);
-                        }
-                    }
-                }
+                store_state(p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state, 0);
             }
         }
         if (has_next) {
-            const float4 scn = reinterpret_cast<const float4*>(stage_n + L.sc_off)[taun];
-            const float vv = load_v(stage_n, taun);
             broadcast_c(scn.y * vv - scn.z * pkr, creg);
 #pragma unroll
             for (int jj = 0; jj < CT2; ++jj) kc[jj] = kn[jj];
+            sct = scn;
         }
         if (tau == kChunk - 1 || !has_next) {
             __syncwarp();
@@ -503,23 +564,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         return;
     }
     // final state(s): the last token always renormalises, so St is the state
-#pragma unroll
-    for (int i = 0; i < RT; ++i) {
-        const int state = TWIN ? (i / HALF) : 0;
-        const int grow = grow_base + (TWIN ? (i % HALF) : i);
-        float* dst = (state == 0 ? p.jobs[job_idx].s_final : p.jobs[job_idx].s_final_twin);
-        if (!dst) continue;
-        dst += head_state;
-#pragma unroll
-        for (int jc = 0; jc < NCH; ++jc) {
-            const int col0 = (cl + NCL * jc) * CH;
-#pragma unroll
-            for (int e4 = 0; e4 < CH / 4; ++e4) {
-                const float2 a0 = S[i][jc * (CH / 2) + e4 * 2 + 0];
-                const float2 a1 = S[i][jc * (CH / 2) + e4 * 2 + 1];
-                reinterpret_cast<float4*>(dst + (size_t)grow * DK + col0)[e4] = make_float4(a0.x, a0.y, a1.x, a1.y);
-            }
-        }
+    float* fin = p.jobs[job_idx].s_final;
+    if (fin) store_state(fin + head_state, 0);
+    if constexpr (TWIN) {
+        float* fin2 = p.jobs[job_idx].s_final_twin;
+        if (fin2) store_state(fin2 + head_state, 1);
     }
 }
 

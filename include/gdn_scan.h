@@ -62,6 +62,16 @@ typedef enum gdn_status {
 
 typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
+/* Which kernel runs the scan.  Both compute the same recurrence in fp32 state
+ * precision; they differ in rounding order only.
+ *  GDN_ALGO_AUTO        chunked when supported (d_k = d_v = 128, bf16 q/k/v),
+ *                       otherwise per-token
+ *  GDN_ALGO_PER_TOKEN   token by token on the FP32 pipes (any supported size)
+ *  GDN_ALGO_CHUNKED     64-token chunks (WY / UT-transform form) on the tensor
+ *                       cores; non-exact operands are split into two bf16 halves
+ *                       with fp32 accumulation.  GDN_ERR_UNSUPPORTED otherwise. */
+typedef enum gdn_algo { GDN_ALGO_AUTO = 0, GDN_ALGO_PER_TOKEN = 1, GDN_ALGO_CHUNKED = 2 } gdn_algo;
+
 typedef struct gdn_problem {
     int32_t num_seqs;            /* B >= 1                                           */
     int32_t num_heads;           /* H >= 1                                           */
@@ -70,6 +80,7 @@ typedef struct gdn_problem {
     const int64_t* cu_seqlens;   /* host [B+1]: 0 = cu[0] <= cu[1] <= ... = T        */
     gdn_dtype qkv_dtype;         /* dtype of q, k, v                                 */
     gdn_dtype out_dtype;         /* dtype of the readout o (rounded to nearest even) */
+    gdn_algo algo;               /* kernel choice (GDN_ALGO_AUTO by default)          */
 } gdn_problem;
 
 /*

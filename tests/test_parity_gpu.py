@@ -103,13 +103,15 @@ def test_tiny_prefill_resume_replay():
 # ---------------------------------------------------------------------------------------------
 # Ragged batches spanning several 32-token tiles with ragged tails, every d_k
 # ---------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("dk,dv,dtype,out", [
-    (64, 64, torch.bfloat16, torch.bfloat16), (64, 64, torch.bfloat16, torch.float32),
-    (128, 128, torch.bfloat16, torch.bfloat16), (128, 128, torch.float32, torch.float32),
-    (32, 32, torch.bfloat16, torch.float32), (128, 64, torch.bfloat16, torch.float32),
-    (64, 128, torch.float32, torch.bfloat16), (32, 128, torch.bfloat16, torch.bfloat16),
+@pytest.mark.parametrize("dk,dv,dtype,out,algo", [
+    (64, 64, torch.bfloat16, torch.bfloat16, "auto"), (64, 64, torch.bfloat16, torch.float32, "auto"),
+    (128, 128, torch.bfloat16, torch.bfloat16, "per_token"), (128, 128, torch.bfloat16, torch.bfloat16, "chunked"),
+    (128, 128, torch.bfloat16, torch.float32, "chunked"),
+    (128, 128, torch.float32, torch.float32, "auto"),
+    (32, 32, torch.bfloat16, torch.float32, "auto"), (128, 64, torch.bfloat16, torch.float32, "auto"),
+    (64, 128, torch.float32, torch.bfloat16, "auto"), (32, 128, torch.bfloat16, torch.bfloat16, "auto"),
 ])
-def test_ragged_prefill_with_initial_state(dk, dv, dtype, out):
+def test_ragged_prefill_with_initial_state(dk, dv, dtype, out, algo):
     lens = [100, 37, 0, 300, 1]
     H = 3
     w, inp = _inputs(11 + dk + dv, lens, H, dk, dv, dtype, 0.85, 1.0)
@@ -117,7 +119,8 @@ def test_ragged_prefill_with_initial_state(dk, dv, dtype, out):
     ck = [[1, 32, 33, 100], [37], [], [64, 65, 299, 300], [1]]
     S0 = synth.state(5, w.B * H, dv, dk, 0.5).view(w.B, H, dv, dk)
     d = _dev(inp)
-    r = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, S0=S0.to(DEV), ckpt_pos=ck, out_dtype=out)
+    r = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, S0=S0.to(DEV), ckpt_pos=ck, out_dtype=out,
+                             algo=algo)
     torch.cuda.synchronize()
     slot = 0
     slots = []
@@ -136,8 +139,8 @@ def test_ragged_prefill_with_initial_state(dk, dv, dtype, out):
     assert torch.equal(r["S_final"][2].cpu(), S0[2])
 
 
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32)])
-def test_ragged_replay_twin_and_readout(dk, dv):
+@pytest.mark.parametrize("dk,dv,algo", [(128, 128, "per_token"), (128, 128, "chunked"), (64, 32, "auto")])
+def test_ragged_replay_twin_and_readout(dk, dv, algo):
     lens = [200, 71, 5, 64]
     H = 4
     w, inp = _inputs(21 + dk, lens, H, dk, dv, torch.bfloat16, 0.9, 1.0)
@@ -147,7 +150,7 @@ def test_ragged_replay_twin_and_readout(dk, dv):
     S_a = synth.state(9, w.B * H, dv, dk, 1.0).view(w.B, H, dv, dk)
     for rn, rd in ((1, 10), (1, 1), (0, 1), (3, 7)):
         rp = gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, rn, rd, S_a=S_a.to(DEV), readout=True,
-                                 out_dtype=torch.float32)
+                                 out_dtype=torch.float32, algo=algo)
         torch.cuda.synchronize()
         for b in range(w.B):
             a_, k_ = oracle.replay_plan(m[b], rn, rd)
@@ -163,7 +166,7 @@ def test_ragged_replay_twin_and_readout(dk, dv):
                 else:
                     assert not torch.any(rp["S_hat"][b, h]), "k = 0 leaves the zero state"
     # state-only replay without the twin
-    rp = gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 10)
+    rp = gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 10, algo=algo)
     torch.cuda.synchronize()
     for b in range(w.B):
         sl = slice(cu[b], cu[b + 1])
@@ -172,7 +175,8 @@ def test_ragged_replay_twin_and_readout(dk, dv):
             assert_close(rp["S_hat"][b, h], o_["S_hat"], f"S_hat(no twin) b={b} h={h}")
 
 
-def test_resume_from_seeded_checkpoints():
+@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+def test_resume_from_seeded_checkpoints(algo):
     """Resume with checkpoint states drawn by the generator (fed to both sides)."""
     lens = [300, 130]
     H, dk, dv = 2, 128, 128
@@ -184,7 +188,7 @@ def test_resume_from_seeded_checkpoints():
     probes = [(0, 0), (0, 49), (0, 50), (0, 51), (0, 300), (1, 0), (1, 1), (1, 63), (1, 130), (0, 289)]
     d = _dev(inp)
     rs = gdn.gdn_resume_from_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ck_states.to(DEV), ck, probes,
-                                  S0=S0.to(DEV), out_dtype=torch.bfloat16)
+                                  S0=S0.to(DEV), out_dtype=torch.bfloat16, algo=algo)
     torch.cuda.synchronize()
     base = [0, 3]
     for i, (s, dd) in enumerate(probes):
@@ -203,7 +207,8 @@ def test_resume_from_seeded_checkpoints():
 # ---------------------------------------------------------------------------------------------
 # invariants on the GPU
 # ---------------------------------------------------------------------------------------------
-def test_identity_gates_leave_state_unchanged():
+@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+def test_identity_gates_leave_state_unchanged(algo):
     lens = [77]
     H, dk, dv = 2, 128, 128
     w, inp = _inputs(41, lens, H, dk, dv, torch.bfloat16)
@@ -211,12 +216,14 @@ def test_identity_gates_leave_state_unchanged():
     d = _dev(inp)
     ones = torch.ones_like(d.alpha)
     zeros = torch.zeros_like(d.beta)
-    r = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, ones, zeros, w.cu_seqlens, S0=S0.to(DEV), out_dtype=torch.float32)
+    r = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, ones, zeros, w.cu_seqlens, S0=S0.to(DEV), out_dtype=torch.float32,
+                             algo=algo)
     torch.cuda.synchronize()
     assert torch.equal(r["S_final"].cpu(), S0), "alpha = 1, beta = 0 must leave S unchanged (bitwise)"
 
 
-def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic():
+@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic(algo):
     """Resume from the deepest stored checkpoint c_j <= d reproduces, bit for bit,
     the state at d of a full run that stores the same checkpoints plus d.  (Each
     stored checkpoint renormalises the running scale, so the comparison run must
@@ -228,15 +235,15 @@ def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic():
     cu = w.cu_seqlens
     C = [321, 500, 777]
     depths = [321, 322, 400, 499, 500, 501, 776, 777, 1000]
-    base = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=[C], readout=False)
-    again = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=[C], readout=False)
+    base = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=[C], readout=False, algo=algo)
+    again = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=[C], readout=False, algo=algo)
     rs = gdn.gdn_resume_from_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, base["ckpt_states"], [C],
-                                  [(0, dd) for dd in depths], readout=False)
+                                  [(0, dd) for dd in depths], readout=False, algo=algo)
     torch.cuda.synchronize()
     assert torch.equal(base["ckpt_states"], again["ckpt_states"]) and torch.equal(base["S_final"], again["S_final"])
     for i, dd in enumerate(depths):
         Cd = sorted(set(C) | {dd})
-        full = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=[Cd], readout=False)
+        full = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=[Cd], readout=False, algo=algo)
         torch.cuda.synchronize()
         assert rs["chosen"][i] == max(c for c in C if c <= dd)
         assert torch.equal(rs["S_out"][i], full["ckpt_states"][Cd.index(dd)]), \
@@ -285,14 +292,16 @@ def _host_head(inp, t0, t1, h, with_q=True):
     return q, inp.k[t0:t1, h].cpu(), inp.v[t0:t1, h].cpu(), inp.alpha[t0:t1, h].cpu(), inp.beta[t0:t1, h].cpu()
 
 
-def test_full_prefill_workload_sampled():
+@pytest.mark.parametrize("algo", ["auto", "per_token"])
+def test_full_prefill_workload_sampled(algo):
     """8 x 16 heads, N = 8192, bf16, 16 equally spaced checkpoints: full run, sampled oracle."""
     w = synth.workload("prefill")
     inp = _gpu_inputs(w)
     cu = w.cu_seqlens
     ck = w.ckpt_positions()
-    r = gdn.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, cu, ckpt_pos=ck)
-    r32 = gdn.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, cu, ckpt_pos=ck, out_dtype=torch.float32)
+    r = gdn.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, cu, ckpt_pos=ck, algo=algo)
+    r32 = gdn.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, cu, ckpt_pos=ck, out_dtype=torch.float32,
+                               algo=algo)
     torch.cuda.synchronize()
     assert torch.equal(r["S_final"], r32["S_final"]), "readout dtype must not change the state"
     assert torch.equal(r["ckpt_states"], r32["ckpt_states"])
