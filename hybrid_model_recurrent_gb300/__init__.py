@@ -77,6 +77,8 @@ def lib():
             L.gdn_read_status.argtypes = [vp, sz, vp]
             L.gdn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.gdn_set_wait_limit_ns.restype = None
+            L.gdn_debug_stall_after.argtypes = [ctypes.c_int32]
+            L.gdn_debug_stall_after.restype = None
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_status_string.restype = ctypes.c_char_p
             for f in ("gdn_prefill_ckpt", "gdn_resume_from_ckpt", "gdn_tail_replay", "gdn_replay_plan",
@@ -148,6 +150,11 @@ def clear_status(device=None, stream=None, ws: Optional[torch.Tensor] = None) ->
 
 def set_wait_limit_ns(ns: int) -> None:
     lib().gdn_set_wait_limit_ns(int(ns))
+
+
+def debug_stall_after(chunks: int) -> None:
+    """Testing hook: later launches stop issuing input copies after `chunks` chunks (-1: off)."""
+    lib().gdn_debug_stall_after(int(chunks))
 
 
 def gdn_replay_plan(m: int, r_num: int, r_den: int):

@@ -21,6 +21,7 @@ namespace {
 
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int32_t> g_stall_after{-1};
 constexpr size_t kWorkspaceBytes = 256;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -195,6 +196,7 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
     prm->ckpt_states = L.ckpt_states;
     prm->status = L.status;
     prm->wait_limit_ns = g_wait_ns.load();
+    prm->stall_after = g_stall_after.load();
     prm->H = H;
     prm->dv = D;
     const bool out_bf16 = p->out_dtype == GDN_BF16;
@@ -241,6 +243,7 @@ gdn_status run_jobs(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_
     prm->ckpt_states = L.ckpt_states;
     prm->status = L.status;
     prm->wait_limit_ns = g_wait_ns.load();
+    prm->stall_after = g_stall_after.load();
     prm->H = H;
     prm->dv = dv;
     prm->nw = nw;
@@ -300,6 +303,8 @@ GDN_EXPORT gdn_status gdn_select_ckpt(const int64_t* c, int32_t M, int64_t d, in
 GDN_EXPORT size_t gdn_workspace_size(void) { return kWorkspaceBytes; }
 
 GDN_EXPORT void gdn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+GDN_EXPORT void gdn_debug_stall_after(int32_t chunks) { g_stall_after.store(chunks < 0 ? -1 : chunks); }
 
 GDN_EXPORT const char* gdn_status_string(gdn_status s) {
     switch (s) {

@@ -200,16 +200,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_kernel(const __grid_con
     Pos cur = next_chunk(0, ck_sched);
     int chunk_no = 0;            // chunks consumed
     int issued = 0;              // chunks whose copies were issued (uniform across threads)
-    if (len > 0 && threadIdx.x == 0) issue(0, 0);
-    if (len > 0) issued = 1;
+    const bool may_issue0 = p.stall_after < 0 || p.stall_after > 0;   // testing hook (see Params)
+    if (len > 0 && may_issue0 && threadIdx.x == 0) issue(0, 0);
+    if (len > 0 && may_issue0) issued = 1;
     float ga0 = 1.f, ga1 = 1.f, gb0 = 0.f, gb1 = 0.f;
     if (len > 0 && warp == 0) load_gates(cur, ga0, ga1, gb0, gb1);
 
     while (len > 0 && cur.begin < len) {
         const int buf = chunk_no & 1;
         const Pos nxt = (cur.begin + cur.len < len) ? next_chunk(cur.begin + cur.len, ck_sched) : Pos{len, 0};
-        if (nxt.len > 0 && threadIdx.x == 0) issue(buf ^ 1, nxt.begin);
-        if (nxt.len > 0) ++issued;
+        const bool may_issue = nxt.len > 0 && issued == chunk_no + 1 && (p.stall_after < 0 || issued < p.stall_after);
+        if (may_issue && threadIdx.x == 0) issue(buf ^ 1, nxt.begin);
+        if (may_issue) ++issued;
         const int clen = cur.len;
         const uint32_t inK = sbase + OFF_IN + buf * kInBytes;
         const uint32_t inQ = inK + kTileBytes;
@@ -654,7 +656,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_kernel(const __grid_con
             for (int cc = chunk_no; cc < issued; ++cc) {
                 const uint64_t t0 = global_ns();
                 while (!mbar_try_wait(&bar[cc & 1], (uint32_t)((cc >> 1) & 1)))
-                    if (global_ns() - t0 > limit) break;
+                    if (global_ns() - t0 > (limit > kDrainLimitNs ? limit : kDrainLimitNs)) break;
             }
             atomicOr(p.status, STATUS_TIMEOUT);
         }

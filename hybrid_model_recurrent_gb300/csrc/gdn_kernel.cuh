@@ -47,6 +47,9 @@ constexpr int kMaxCkpts = 1536;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kSlotsPerWarp = 16;   // state rows (slots) held by one consumer warp
 constexpr float kRenormFloor = 0x1p-32f;
+// Bound of the wait for this CTA's own copies in flight before it exits (independent of the
+// user's wait limit, so that even a tiny limit never lets a CTA leave with a copy pending).
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 enum : uint32_t { FLAG_RENORM = 1u, FLAG_DUMP = 2u, FLAG_INDEX_SHIFT = 8u };
 enum : unsigned { STATUS_TIMEOUT = 1u };
@@ -87,6 +90,8 @@ struct Params {
     int32_t rows_per_cta;   // real state rows per CTA
     int32_t ctas_per_head;  // dv / rows_per_cta
     int32_t n_jobs;
+    int32_t stall_after;    // testing hook: stop issuing input copies after this many chunks (-1: off)
+    int32_t pad_;
     Job jobs[kMaxJobs];
     Ckpt ckpts[kMaxCkpts];
 };
@@ -280,6 +285,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
             const int st = c % kStages;
+            if (p.stall_after >= 0 && c >= p.stall_after) break;   // testing hook (see Params)
             if (c >= kStages && !warp_wait(&empty[st], (uint32_t)(((c / kStages) + 1) & 1), limit)) {
                 ok = false;
                 break;
@@ -362,7 +368,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
         // never leave with copies in flight into this CTA's shared memory
         for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
-            warp_wait(IN_BF16 ? &rawb[c % kStages] : &full[c % kStages], (uint32_t)((c / kStages) & 1), limit);
+            warp_wait(IN_BF16 ? &rawb[c % kStages] : &full[c % kStages], (uint32_t)((c / kStages) & 1),
+                      limit > kDrainLimitNs ? limit : kDrainLimitNs);
         if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
         return;
     }

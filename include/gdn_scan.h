@@ -224,6 +224,14 @@ gdn_status gdn_read_status(const void* workspace, size_t ws_bytes, gdn_stream_t 
  * from this process (default 2 s; 0 restores the default). */
 void gdn_set_wait_limit_ns(uint64_t ns);
 
+/* Testing hook for failure detection: kernels launched afterwards from this
+ * process stop issuing their input copies after `chunks` chunks (of 32 tokens
+ * per-token, 64 chunked), so the next wait of each CTA can only run out; the
+ * CTA then drains its own copies, records GDN_ERR_DEVICE_TIMEOUT in the
+ * workspace and returns (outputs are incomplete).  Negative disables (the
+ * default).  Pair it with a short gdn_set_wait_limit_ns. */
+void gdn_debug_stall_after(int32_t chunks);
+
 /* Human-readable name of a status code. */
 const char* gdn_status_string(gdn_status s);
 
