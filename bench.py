@@ -50,11 +50,12 @@ SM_MAX_MHZ = 2070.0
 PEAK_ALU_TFLOPS = SM_COUNT * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12  # 80.54
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_prefill_8x16x8192.md")
-KERNEL_SRC = os.path.join(ROOT, "hybrid_model_recurrent_gb300", "csrc", "gdn_chunk.cuh")
-# mma.sync m16n8k16 instructions per warp per 64-token chunk in the chunked kernel (8 warps,
-# 2048 MAC each): K K^T / Q K^T 64, blocked substitution 152, U and Q S_0^T 320, P U 96, update 128
-CHUNK_MMA_PER_WARP = 760
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_chunk_tc_kernel_prefill_8x16x8192.md")
+KERNEL_SRC = os.path.join(ROOT, "hybrid_model_recurrent_gb300", "csrc", "gdn_chunk_tc.cuh")
+# tcgen05.mma MACs per 64-token chunk and head in the chunked kernel: 76 MMAs of 128x64x16
+# ([K;Q] K^T 8, W^T and U~^T 16, S_0 (-W)^T and S_0 Q^T 40, U''^T P''^T 12) and 8 of 128x128x16
+# (the state update)
+CHUNK_MACS = 76 * 128 * 64 * 16 + 8 * 128 * 128 * 16
 
 
 def measured_peaks():
@@ -404,7 +405,7 @@ def run_ours(args, ws, rank, local):
     achieved_gbs = bytes_per_launch / (prefill_ms * 1e-3) / 1e9
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     chunks = w.B * w.H * ((w.seq_lens[0] + 63) // 64)
-    mma_flops = chunks * 8 * CHUNK_MMA_PER_WARP * 2048 * 2
+    mma_flops = chunks * CHUNK_MACS * 2
     base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
     if rank == 0:
         line = {
@@ -415,7 +416,7 @@ def run_ours(args, ws, rank, local):
             "e2e": {"value": e2e_thr / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
             "gpu_launches": step.launches_per_step * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "gdn_chunk_kernel<bf16 out, readout> (prefill)",
+            "roofline": {"bound": "hbm", "kernel": "gdn_chunk_tc_kernel<bf16 out, readout> (prefill)",
                          "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved_gbs / hbm_peak, "traffic": profile_traffic(),
                          "launch_ms": prefill_ms, "algorithmic_bytes_per_launch": bytes_per_launch,

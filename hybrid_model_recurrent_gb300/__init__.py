@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn_scan.so")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = range(5)
 GDN_F32, GDN_BF16 = 0, 1
-ALGO = {"auto": 0, "per_token": 1, "chunked": 2}
+ALGO = {"auto": 0, "per_token": 1, "chunked": 2, "chunked_mma": 3}
 
 _lock = threading.Lock()
 _lib = None

@@ -13,6 +13,7 @@
 
 #include "../../include/gdn_scan.h"
 #include "gdn_chunk.cuh"
+#include "gdn_chunk_tc.cuh"
 #include "gdn_kernel.cuh"
 
 #define GDN_EXPORT extern "C" __attribute__((visibility("default")))
@@ -76,10 +77,11 @@ gdn_status check_problem(const gdn_problem* p, std::vector<int64_t>& lens) {
     if (p->num_seqs < 1 || p->num_heads < 1 || p->d_k < 1 || p->d_v < 1) return GDN_ERR_INVALID_ARG;
     if ((p->qkv_dtype != GDN_F32 && p->qkv_dtype != GDN_BF16) || (p->out_dtype != GDN_F32 && p->out_dtype != GDN_BF16))
         return GDN_ERR_INVALID_ARG;
-    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_PER_TOKEN && p->algo != GDN_ALGO_CHUNKED)
+    if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_PER_TOKEN && p->algo != GDN_ALGO_CHUNKED &&
+        p->algo != GDN_ALGO_CHUNKED_MMA)
         return GDN_ERR_INVALID_ARG;
     if (!supported_d(p->d_k) || !supported_d(p->d_v)) return GDN_ERR_UNSUPPORTED;
-    if (p->algo == GDN_ALGO_CHUNKED && !chunked_ok(p)) return GDN_ERR_UNSUPPORTED;
+    if ((p->algo == GDN_ALGO_CHUNKED || p->algo == GDN_ALGO_CHUNKED_MMA) && !chunked_ok(p)) return GDN_ERR_UNSUPPORTED;
     if (p->cu_seqlens[0] != 0) return GDN_ERR_INVALID_ARG;
     lens.resize(p->num_seqs);
     for (int b = 0; b < p->num_seqs; ++b) {
@@ -159,7 +161,8 @@ gdn_status launch_batches(gdn::Params& prm, std::vector<HostJob>& jobs, F&& laun
     return GDN_OK;
 }
 
-// Chunked tensor-core path (d_k = d_v = 128, bf16): one CTA per (job, head).
+// Chunked tensor-core paths (d_k = d_v = 128, bf16): one CTA per (job, head); tcgen05 by default,
+// warp-level mma.sync for GDN_ALGO_CHUNKED_MMA.
 gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_t stream) {
     const gdn_problem* p = L.p;
     const int H = p->num_heads;
@@ -200,8 +203,10 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
     prm->H = H;
     prm->dv = D;
     const bool out_bf16 = p->out_dtype == GDN_BF16;
+    const bool warp_mma = p->algo == GDN_ALGO_CHUNKED_MMA;
     return launch_batches(*prm, jobs, [&](const gdn::Params& pr, int nj) -> cudaError_t {
         const int grid = nj * H;
+        if (!warp_mma) return gdn::tc::launch(pr, grid, L.readout, out_bf16, stream);
         if (L.readout)
             return out_bf16 ? gdn::chunk::launch_chunk<true, true>(pr, grid, stream)
                             : gdn::chunk::launch_chunk<false, true>(pr, grid, stream);

@@ -1,0 +1,14 @@
+// inst_chunk_tc.cu - instantiations of the tcgen05 chunkwise kernel (own translation unit so
+// that it compiles in parallel with the rest of the library).
+#include "gdn_chunk_tc.cuh"
+
+namespace gdn {
+namespace tc {
+
+cudaError_t launch(const Params& p, int grid, bool readout, bool out_bf16, cudaStream_t stream) {
+    if (readout) return out_bf16 ? launch_chunk_tc<true, true>(p, grid, stream) : launch_chunk_tc<false, true>(p, grid, stream);
+    return launch_chunk_tc<false, false>(p, grid, stream);
+}
+
+}  // namespace tc
+}  // namespace gdn

@@ -62,15 +62,28 @@ typedef enum gdn_status {
 
 typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
-/* Which kernel runs the scan.  Both compute the same recurrence in fp32 state
+/* Which kernel runs the scan.  All compute the same recurrence in fp32 state
  * precision; they differ in rounding order only.
- *  GDN_ALGO_AUTO        chunked when supported (d_k = d_v = 128, bf16 q/k/v),
- *                       otherwise per-token
- *  GDN_ALGO_PER_TOKEN   token by token on the FP32 pipes (any supported size)
- *  GDN_ALGO_CHUNKED     64-token chunks (WY / UT-transform form) on the tensor
- *                       cores; non-exact operands are split into two bf16 halves
- *                       with fp32 accumulation.  GDN_ERR_UNSUPPORTED otherwise. */
-typedef enum gdn_algo { GDN_ALGO_AUTO = 0, GDN_ALGO_PER_TOKEN = 1, GDN_ALGO_CHUNKED = 2 } gdn_algo;
+ *  GDN_ALGO_AUTO         GDN_ALGO_CHUNKED when supported (d_k = d_v = 128, bf16
+ *                        q/k/v), otherwise per-token
+ *  GDN_ALGO_PER_TOKEN    token by token on the FP32 pipes (any supported size)
+ *  GDN_ALGO_CHUNKED      chunks of up to 64 tokens (WY / UT-transform form) on the
+ *                        5th-generation tensor cores (tcgen05, accumulators and
+ *                        state in tensor memory); non-exact operands are split into
+ *                        two bf16 halves with fp32 accumulation.  A chunk also ends
+ *                        where the decay product within it would fall below 2^-32,
+ *                        so every alpha in (0, 1] is handled.
+ *  GDN_ALGO_CHUNKED_MMA  the same chunkwise form on warp-level mma.sync, 64-token
+ *                        chunks only: the decay product over one chunk must stay
+ *                        above 2^-126 (alpha^64 > 1.2e-38), else results are not
+ *                        finite.
+ * The two chunked algorithms return GDN_ERR_UNSUPPORTED for other sizes. */
+typedef enum gdn_algo {
+    GDN_ALGO_AUTO = 0,
+    GDN_ALGO_PER_TOKEN = 1,
+    GDN_ALGO_CHUNKED = 2,
+    GDN_ALGO_CHUNKED_MMA = 3
+} gdn_algo;
 
 typedef struct gdn_problem {
     int32_t num_seqs;            /* B >= 1                                           */

@@ -71,12 +71,13 @@ def _vp(off=0):
     return ctypes.c_void_p(FAKE + off)
 
 
-def _prob(B=2, H=2, dk=32, dv=32, cu=(0, 10, 30), qkv=gdn.GDN_BF16, out=gdn.GDN_BF16):
+def _prob(B=2, H=2, dk=32, dv=32, cu=(0, 10, 30), qkv=gdn.GDN_BF16, out=gdn.GDN_BF16, algo=0):
     arr = np.ascontiguousarray(np.asarray(cu, dtype=np.int64))
     pr = gdn._Problem()
     pr.num_seqs, pr.num_heads, pr.d_k, pr.d_v = B, H, dk, dv
     pr.cu_seqlens = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
     pr.qkv_dtype, pr.out_dtype = qkv, out
+    pr.algo = algo
     return pr, arr
 
 
@@ -103,6 +104,11 @@ def test_prefill_rejects_bad_arguments(L):
     assert prefill(L, _prob(cu=(0, 10, 5))[0]) == E           # decreasing cu_seqlens
     assert prefill(L, _prob(cu=(1, 10, 30))[0]) == E           # cu_seqlens[0] != 0
     assert prefill(L, _prob(qkv=7)[0]) == E
+    assert prefill(L, _prob(algo=4)[0]) == E                    # unknown algorithm
+    assert prefill(L, _prob(algo=-1)[0]) == E
+    for a in (gdn.ALGO["chunked"], gdn.ALGO["chunked_mma"]):
+        assert prefill(L, _prob(algo=a)[0]) == U                # chunked needs d_k = d_v = 128 and bf16
+        assert prefill(L, _prob(dk=128, dv=128, qkv=gdn.GDN_F32, algo=a)[0]) == U
     assert prefill(L, pr, k=None) == E
     assert prefill(L, pr, q=None) == E                          # readout requested without q
     assert prefill(L, pr, k=_vp(0x1008)) == E                   # k not 16-byte aligned
@@ -127,6 +133,9 @@ def test_prefill_valid_call_without_gpu_reports_cuda_error(L):
     pr, _keep = _prob()
     # arguments are valid: the library gets as far as CUDA, which is absent here
     assert prefill(L, pr, pos=[5, 10, 7], cu=[0, 2, 3]) == gdn.GDN_ERR_CUDA
+    for a in gdn.ALGO.values():
+        pr2, _k2 = _prob(dk=128, dv=128, algo=a)
+        assert prefill(L, pr2, pos=[5, 10, 7], cu=[0, 2, 3]) == gdn.GDN_ERR_CUDA
 
 
 def test_resume_and_replay_reject_bad_arguments(L):

@@ -106,7 +106,7 @@ def test_tiny_prefill_resume_replay():
 @pytest.mark.parametrize("dk,dv,dtype,out,algo", [
     (64, 64, torch.bfloat16, torch.bfloat16, "auto"), (64, 64, torch.bfloat16, torch.float32, "auto"),
     (128, 128, torch.bfloat16, torch.bfloat16, "per_token"), (128, 128, torch.bfloat16, torch.bfloat16, "chunked"),
-    (128, 128, torch.bfloat16, torch.float32, "chunked"),
+    (128, 128, torch.bfloat16, torch.float32, "chunked"), (128, 128, torch.bfloat16, torch.bfloat16, "chunked_mma"),
     (128, 128, torch.float32, torch.float32, "auto"),
     (32, 32, torch.bfloat16, torch.float32, "auto"), (128, 64, torch.bfloat16, torch.float32, "auto"),
     (64, 128, torch.float32, torch.bfloat16, "auto"), (32, 128, torch.bfloat16, torch.bfloat16, "auto"),
@@ -139,7 +139,8 @@ def test_ragged_prefill_with_initial_state(dk, dv, dtype, out, algo):
     assert torch.equal(r["S_final"][2].cpu(), S0[2])
 
 
-@pytest.mark.parametrize("dk,dv,algo", [(128, 128, "per_token"), (128, 128, "chunked"), (64, 32, "auto")])
+@pytest.mark.parametrize("dk,dv,algo", [(128, 128, "per_token"), (128, 128, "chunked"), (128, 128, "chunked_mma"),
+                                        (64, 32, "auto")])
 def test_ragged_replay_twin_and_readout(dk, dv, algo):
     lens = [200, 71, 5, 64]
     H = 4
@@ -175,7 +176,7 @@ def test_ragged_replay_twin_and_readout(dk, dv, algo):
             assert_close(rp["S_hat"][b, h], o_["S_hat"], f"S_hat(no twin) b={b} h={h}")
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma"])
 def test_resume_from_seeded_checkpoints(algo):
     """Resume with checkpoint states drawn by the generator (fed to both sides)."""
     lens = [300, 130]
@@ -204,10 +205,73 @@ def test_resume_from_seeded_checkpoints(algo):
                 check_output(rs["o"][lo:hi, h], o_["o"], f"resume o probe {i} h={h}")
 
 
+def _small_alpha_inputs(seed, lens, H):
+    """bf16 d = 128 streams whose gates reach down to the bottom of the supported range:
+    about 6% of the tokens take alpha = 10^(-30 u) (1 down to 1e-30), and a run of tokens
+    takes alpha ~ U[0.2, 0.5], so that decay products cross 2^-32 inside a 64-token window."""
+    w, inp = _inputs(seed, lens, H, 128, 128, torch.bfloat16, 0.85, 1.0)
+    u, _ = synth.gates(seed + 1000, 0, w.T, H, 0.0, 1.0, "uniform")
+    sel, _ = synth.gates(seed + 2000, 0, w.T, H, 0.0, 1.0, "uniform")
+    mid, _ = synth.gates(seed + 3000, 0, w.T, H, 0.2, 0.5, "uniform")
+    alpha = inp.alpha.clone()
+    alpha[100:180] = mid[100:180]
+    tiny = sel < 0.06
+    alpha[tiny] = torch.pow(10.0, -30.0 * u[tiny].double()).float()
+    alpha = torch.clamp(alpha, min=1e-30)
+    return w, synth.Inputs(inp.q, inp.k, inp.v, alpha, inp.beta)
+
+
+@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+def test_small_alpha_gates(algo):
+    """alpha down to 1e-30 (the bottom of the documented range), with checkpoints and a resume."""
+    lens = [300, 129]
+    H = 2
+    w, inp = _small_alpha_inputs(61, lens, H)
+    assert float(inp.alpha.min()) < 1e-25 and float(inp.alpha.max()) <= 1.0
+    cu = w.cu_seqlens
+    ck = [[64, 101, 150, 299], [1, 128]]
+    S0 = synth.state(19, w.B * H, 128, 128, 0.5).view(w.B, H, 128, 128)
+    d = _dev(inp)
+    r = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, S0=S0.to(DEV), ckpt_pos=ck,
+                             out_dtype=torch.float32, algo=algo)
+    torch.cuda.synchronize()
+    slots = [[0, 1, 2, 3], [4, 5]]
+    refs = {}
+    for b in range(w.B):
+        for h in range(H):
+            ref = _oracle_prefill_head(inp, cu, b, h, S0=S0[b, h], ckpt=ck[b])
+            refs[b, h] = ref
+            assert_close(r["S_final"][b, h], ref["S"], f"S_N b={b} h={h}")
+            check_output(r["o"][cu[b]:cu[b + 1], h], ref["o"], f"o b={b} h={h}")
+            for i, s in enumerate(slots[b]):
+                assert_close(r["ckpt_states"][s, h], ref["ckpt"][i], f"ckpt b={b} c={ck[b][i]} h={h}")
+    # resume from the oracle's checkpoint states (fp32), fed to both sides
+    ck_states = torch.zeros(6, H, 128, 128, dtype=torch.float32)
+    for b in range(w.B):
+        for h in range(H):
+            for i, s in enumerate(slots[b]):
+                ck_states[s, h] = torch.as_tensor(np.asarray(refs[b, h]["ckpt"][i]), dtype=torch.float32)
+    probes = [(0, 120), (0, 300), (1, 77)]
+    rs = gdn.gdn_resume_from_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ck_states.to(DEV), ck, probes,
+                                  S0=S0.to(DEV), out_dtype=torch.float32, algo=algo)
+    torch.cuda.synchronize()
+    for i, (s, dd) in enumerate(probes):
+        sl = slice(cu[s], cu[s + 1])
+        for h in range(H):
+            st = [ck_states[slots[s][j], h] for j in range(len(ck[s]))]
+            o_ = oracle.resume(inp.q[sl, h], inp.k[sl, h], inp.v[sl, h], inp.alpha[sl, h], inp.beta[sl, h],
+                               st, ck[s], dd, S0=S0[s, h])
+            assert rs["chosen"][i] == o_["c"]
+            assert_close(rs["S_out"][i, h], o_["S"], f"small-alpha resume probe {i} h={h}")
+            lo, hi = rs["offsets"][i], rs["offsets"][i + 1]
+            if hi > lo:
+                check_output(rs["o"][lo:hi, h], o_["o"], f"small-alpha resume o probe {i} h={h}")
+
+
 # ---------------------------------------------------------------------------------------------
 # invariants on the GPU
 # ---------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma"])
 def test_identity_gates_leave_state_unchanged(algo):
     lens = [77]
     H, dk, dv = 2, 128, 128
@@ -222,7 +286,7 @@ def test_identity_gates_leave_state_unchanged(algo):
     assert torch.equal(r["S_final"].cpu(), S0), "alpha = 1, beta = 0 must leave S unchanged (bitwise)"
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma"])
 def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic(algo):
     """Resume from the deepest stored checkpoint c_j <= d reproduces, bit for bit,
     the state at d of a full run that stores the same checkpoints plus d.  (Each
