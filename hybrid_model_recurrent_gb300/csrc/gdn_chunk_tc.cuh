@@ -13,27 +13,39 @@
 //
 // Every product is one tcgen05.mma with M = 128: the state rows (d_v) or the stacked [K; Q] rows.
 // The state lives in TMEM as S = sigma St for the whole job.  With sigma_n = sigma_0 gamma_n and
-// U''_s = c_s u_s, c_s = 1/(sigma_0 gamma_s), the update is St_n = St_0 + U''^T K (the accumulator
-// is never rescaled per chunk) and the readout is o_t = gamma_t (S_0 Q^T)[:, t] + (U''^T P''^T)[:, t]
-// with P''[t][s] = sigma_0 gamma_t (q_t.k_s).  What keeps every factor finite:
-//   * a chunk ends before the token at which gamma would fall below 2^-32, so gamma_s >= 2^-32;
-//   * a chunk of one token with alpha < 2^-32 first scales St to alpha_1 S_0 (sigma -> 1) and then
-//     takes c = 1 and P'' = q.k, so no factor exceeds 1;
+// U''_s = c_s u_s, c_s = 1/(sigma_0 gamma_s):
+//   U^T    = U~^T + St (-sigma_0 W)^T                (S_0 = sigma_0 St)
+//   St_n   = St_0 + U''^T K                           (the accumulator is never rescaled per chunk)
+//   o_t    = sigma_0 gamma_t (St Q^T + U''^T P^T)[:, t],  P[t][s] = q_t.k_s for s <= t
+// What keeps every factor finite for any alpha in (0, 1]:
+//   * a chunk ends before the token at which gamma would fall below 2^-32, so 1/gamma <= 2^32;
+//   * a chunk of one token with alpha < 2^-32 scales St to alpha_1 S_0 / 1 (sigma -> 1) before its
+//     update, takes c = 1, and reads out o_1 = sigma_0 alpha_1 St q_1 + (q_1.k_1) u_1 directly;
 //   * sigma is folded into St (St <- sigma St, sigma <- 1) when it falls below 2^-40, at every
 //     checkpoint and at the end, so checkpoints are plain states and a resume from one repeats
 //     the full run's arithmetic bit for bit.
 // Chunk ends depend only on the checkpoint list and on the gates after the previous chunk end,
 // which the full run and a resume see alike.
 //
-// Operands that are not exact in bf16 (T diag(.), W, U'', P'', S_0) are split x = hi + lo into two
+// Operands that are not exact in bf16 (T diag(.), W, U'', P, St) are split x = hi + lo into two
 // bf16 halves and multiplied as hi*hi + hi*lo + lo*hi (or hi*x + lo*x against the exact q, k, v),
 // accumulated in fp32 in TMEM.
 //
+// Three warp roles run a software pipeline over the chunks of one (job, head):
+//   chain (warps 0-3) - the state-dependent conversions of chunk j: St into the bf16 A operand,
+//       U'' from U, readout, checkpoints;
+//   prep (warps 4-11) - the state-independent conversions of chunk j+1: L from G, T, the
+//       T diag(.) operands, -sigma_0 W, P, and (one warp) the gates and the chunk schedule one
+//       chunk further ahead;
+//   issue (warp 12, one lane) - every tcgen05.mma: the chain's U^T += St (-sigma_0 W)^T, St Q^T,
+//       St += U''^T K, U''^T P^T and the prep's G = [K; Q] K^T, W^T, U~^T, each as soon as the
+//       mbarriers of its operands have fired, so that no converting warp waits on a full MMA queue.
+// They hand over through mbarriers; each group agrees on every wait by a barrier reduction, so a
+// wait that runs out ends every loop without leaving a named barrier half-entered.
+//
 // TMEM (512 columns x 128 lanes of 32 bit):
-//   [0,128) St   [128,192) U^T   [192,256) S_0 Q^T   [256,320) G, then U''^T P''^T   [320,384) W^T
-//   [384,448) S_0 hi (bf16 pairs)   [448,512) S_0 lo
-// Thread 0 issues the TMA copies and the MMAs; warp w reaches TMEM lanes 32(w%4)..+31, and warps
-// w and w+4 split the columns.
+//   [0,128) St   [128,192) U^T   [192,256) O^T   [256,320) G   [320,384) W^T
+//   [384,448) St hi (bf16 pairs)   [448,512) St lo
 #pragma once
 
 #include "gdn_kernel.cuh"
@@ -43,35 +55,49 @@ namespace tc {
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NTHREADS = 256;
+constexpr int NCHAIN = 128;                  // warps 0-3
+constexpr int NPREP = 256;                   // warps 4-11
+constexpr int NTHREADS = NCHAIN + NPREP + 32;   // + warp 12: MMA issue
+constexpr int BAR_CHAIN = 1, BAR_PREP = 2, BAR_PREP_A = 3;   // named barriers (3 and 4: halves of prep)
+constexpr int kRing = 4;                     // chunk schedule entries in flight
 
 struct Pos {   // chunk schedule cursor
     int begin, len;
 };
 
+// Per-chunk schedule and scalars, written by the gate warp, read by both groups.
+struct Ring {
+    int begin, n, single, fold, dump_slot, last, next_begin, next_len;
+    float sigma0, sigma_after, prescale, qk0;
+    int pad_[4];
+    float rs[C];   // readout scale sigma_0 gamma_t (single: sigma_0 alpha_1)
+    float c[C];    // U'' scale 1/(sigma_0 gamma_t) (single: 1); 0 past the chunk
+};
+static_assert(sizeof(Ring) == 576, "Ring layout");
+
 // ---- shared memory (bytes); swizzled operand tiles are 1024-aligned ----
-constexpr int OFF_IN = 0;              // 2 x 32 KB: [K;Q] as two 64-column blocks of [128 rows][128 B]
+constexpr int OFF_KQ = 0;              // 2 x 32 KB: [K;Q] as two 64-column blocks of [128 rows][128 B]
 constexpr int OFF_V = 65536;           // 16 KB: V as two 64-column blocks of [64 rows][128 B]
 constexpr int OFF_T1H = 81920;         // [64 t][64 s] bf16 (T diag(beta gamma)) hi
 constexpr int OFF_T1L = 90112;         //   lo
 constexpr int OFF_T2H = 98304;         // (T diag(beta)) hi
 constexpr int OFF_T2L = 106496;        //   lo
-constexpr int OFF_PH = 114688;         // [64 t][64 s] P'' hi
+constexpr int OFF_PH = 114688;         // [64 t][64 s] P hi
 constexpr int OFF_PL = 122880;         //   lo
-constexpr int OFF_WH = 131072;         // [128 dk][64 t] -W^T hi (MN-major B operand)
+constexpr int OFF_WH = 131072;         // [128 dk][64 t] -sigma_0 W^T hi (MN-major B operand)
 constexpr int OFF_WL = 147456;         //   lo
 constexpr int OFF_UH = 163840;         // [128 dv][64 t] U''^T hi (K-major A operand)
 constexpr int OFF_UL = 180224;         //   lo
 constexpr int OFF_LF = 196608;         // fp32 [64][68]: L, then T in place
-constexpr int OFF_LD = 214016;         // fp32 4 x [16][17]: diagonal blocks of L
-constexpr int OFF_Y = 218368;          // fp32 [32][33] scratch
-constexpr int OFF_SC = 222592;         // fp32 per-token scalars: g, ginv, bg, b, c, pscale (6 x 64)
-constexpr int OFF_BAR = 224128;        // mbarriers, TMEM address, chunk schedule
-constexpr int kSmemBytes = OFF_BAR + 128 + 1024;
+constexpr int OFF_LD = 214016;         // fp32 4 x [16][17] diagonal blocks of L; later [32][33] scratch
+constexpr int OFF_PSC = 218368;        // fp32 prep scalars [2][4][64]: gamma, 1/gamma, beta gamma, beta
+constexpr int OFF_RING = 220416;       // Ring[kRing]
+constexpr int OFF_BAR = OFF_RING + kRing * 576;
+constexpr int kBarBytes = 256;
+constexpr int kSmemBytes = OFF_BAR + kBarBytes + 1024;
 constexpr int kLdF = 68;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
-static_assert(OFF_SC + 6 * C * 4 <= OFF_BAR, "scalar area");
-static_assert(OFF_Y + 32 * 33 * 4 <= OFF_SC, "scratch area");
+static_assert(OFF_PSC + 2 * 4 * C * 4 == OFF_RING, "scalar area");
 
 constexpr uint32_t T_S = 0, T_U = 128, T_O = 192, T_G = 256, T_W = 320, T_SH = 384, T_SL = 448;
 constexpr float kGammaFloor = 0x1p-32f;   // smallest in-chunk decay product
@@ -167,6 +193,58 @@ __device__ __forceinline__ void st_split32(unsigned char* th, unsigned char* tl,
         *reinterpret_cast<uint4*>(tl + sw128(row, c0 + 8 * q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
 }
+__device__ __forceinline__ void group_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// barrier over a warp group that also returns whether every thread passed `v`
+__device__ __forceinline__ bool group_all(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+// bounded wait for the phase of `parity`; gives up when another role has given up
+__device__ __forceinline__ bool wait_phase(uint64_t* b, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(b, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > limit) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+// wait by one poller while the rest of the group sleeps in the barrier; afterwards every thread
+// observes the completed phase itself (one probe that succeeds at once), for its own acquire
+__device__ __forceinline__ bool group_wait(uint64_t* b, uint32_t parity, bool poller, int id, int n,
+                                           volatile int* abort_flag, uint64_t limit) {
+    bool ok = true;
+    if (poller) ok = wait_phase(b, parity, abort_flag, limit);
+    ok = group_all(id, n, ok);
+    if (ok) (void)mbar_try_wait(b, parity);
+    return ok;
+}
+// non-blocking probe (try_wait may suspend the thread for a while; a poller over several barriers
+// must not wait on one of them)
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void drain_phase(uint64_t* b, uint32_t parity, uint64_t limit) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(b, parity))
+        if (global_ns() - t0 > limit) break;
+}
 
 // ------------------------------------------------------------------------------------
 // the kernel: one CTA = one (job, head)
@@ -178,25 +256,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    uint64_t* bar_in = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [2]: K/Q buffers
-    uint64_t* bar_v = bar_in + 2;                                       // V buffer
-    uint64_t* bar_mma = bar_in + 3;                                     // tcgen05.commit
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 64);
-    int* sh_sched = reinterpret_cast<int*>(smem + OFF_BAR + 72);        // n, single, next begin, next len
-    float* sc_g = reinterpret_cast<float*>(smem + OFF_SC);
-    float* sc_ginv = sc_g + C;
-    float* sc_bg = sc_ginv + C;
-    float* sc_b = sc_bg + C;
-    float* sc_c = sc_b + C;
-    float* sc_p = sc_c + C;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    // TMA and MMA completions (one arrival each)
+    uint64_t* bar_kq = bars + 0;       // [2] K/Q tiles landed
+    uint64_t* bar_v = bars + 2;        // V tile landed
+    uint64_t* bar_g = bars + 3;        // G done
+    uint64_t* bar_wu = bars + 4;       // W^T, U~^T done
+    uint64_t* bar_uo = bars + 5;       // U^T done
+    uint64_t* bar_st = bars + 6;       // state update and every MMA issued before it done
+    uint64_t* bar_o = bars + 7;        // St Q^T + U''^T P^T done
+    // operands ready for the issuing warp, or results read
+    uint64_t* bar_gin = bars + 8;      // prep: K/Q/V tiles padded, G columns free           (1 arrival)
+    uint64_t* bar_wuin = bars + 9;     // prep: T diag(.) operands in shared memory           (1)
+    uint64_t* bar_wready = bars + 10;  // prep: -sigma_0 W in shared memory                   (NPREP)
+    uint64_t* bar_pready = bars + 11;  // prep: P in shared memory                            (NPREP)
+    uint64_t* bar_split = bars + 12;   // chain: St split into TMEM (and prescaled)           (NCHAIN)
+    uint64_t* bar_ofree = bars + 13;   // chain: O^T read out                                 (NCHAIN)
+    uint64_t* bar_ufree = bars + 14;   // chain: U'' in shared memory, U^T columns free       (NCHAIN)
+    uint64_t* bar_ring = bars + 15;    // [kRing] schedule entry written by the gate warp     (32)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 160);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 164);
+    int* cnt = reinterpret_cast<int*>(smem + OFF_BAR + 168);   // K/Q, V chunks issued; commits g, wu, uo, st, o
+    Ring* ring = reinterpret_cast<Ring*>(smem + OFF_RING);
+    float* psc = reinterpret_cast<float*>(smem + OFF_PSC);
     float* Lf = reinterpret_cast<float*>(smem + OFF_LF);
     float* Ld = reinterpret_cast<float*>(smem + OFF_LD);
-    float* Yb = reinterpret_cast<float*>(smem + OFF_Y);
+    float* Yb = Ld;   // the diagonal blocks are consumed before the merge scratch is written
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lq = warp & 3;                 // TMEM lane quarter of this warp
     const int row = 32 * lq + lane;          // TMEM lane = accumulator row
-    const int half = warp >> 2;              // column half handled by this warp
     const int job_idx = blockIdx.x / p.H;
     const int h = blockIdx.x - job_idx * p.H;
     const int H = p.H;
@@ -216,10 +305,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        mbar_init(&bar_in[0], 1);
-        mbar_init(&bar_in[1], 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_mma, 1);
+        for (int i = 0; i < 10; ++i) mbar_init(&bars[i], 1);
+        mbar_init(bar_wready, NPREP);
+        mbar_init(bar_pready, NPREP);
+        mbar_init(bar_split, NCHAIN);
+        mbar_init(bar_ofree, NCHAIN);
+        mbar_init(bar_ufree, NCHAIN);
+        for (int i = 0; i < kRing; ++i) mbar_init(&bar_ring[i], 32);
+        *abort_flag = 0;
+        for (int i = 0; i < 7; ++i) cnt[i] = 0;
         fence_barrier_init();
     }
     tc_fence_before();
@@ -228,134 +322,259 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     const uint32_t tbase = *tslot;
     const uint32_t trow = tbase + ((uint32_t)(32 * lq) << 16);   // this warp's lane quarter
 
-    // ---- initial state into TMEM: St = S_0, sigma = 1 ----
-    {
-        const float* s0 = job.s0;
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-            const int c0 = 64 * half + 32 * cb;
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (s0) x = __ldg(reinterpret_cast<const float4*>(s0 + head_state + (size_t)row * D + c0 + i));
-                v[i] = x.x;
-                v[i + 1] = x.y;
-                v[i + 2] = x.z;
-                v[i + 3] = x.w;
-            }
-            tmem_st32(trow + T_S + c0, v);
-        }
-        tmem_st_wait();
-    }
-
-    auto issue_kq = [&](int buf, int pos) {   // thread 0
+    auto allowed = [&](int c) { return p.stall_after < 0 || c < p.stall_after; };   // testing hook
+    auto issue_kq = [&](int c, int pos) {
+        const int buf = c & 1;
         proxy_fence();
-        mbar_arrive_expect_tx(&bar_in[buf], 4u * 8192u);
-        unsigned char* dst = smem + OFF_IN + buf * 32768;
+        mbar_arrive_expect_tx(&bar_kq[buf], 4u * 8192u);
+        unsigned char* dst = smem + OFF_KQ + buf * 32768;
         const int t0 = (int)(tok_begin + pos);
-        tma_load_3d(dst + 0, &p.tm_k, 0, h, t0, &bar_in[buf]);
-        tma_load_3d(dst + 8192, &p.tm_q, 0, h, t0, &bar_in[buf]);
-        tma_load_3d(dst + 16384, &p.tm_k, 64, h, t0, &bar_in[buf]);
-        tma_load_3d(dst + 16384 + 8192, &p.tm_q, 64, h, t0, &bar_in[buf]);
+        tma_load_3d(dst + 0, &p.tm_k, 0, h, t0, &bar_kq[buf]);
+        tma_load_3d(dst + 8192, &p.tm_q, 0, h, t0, &bar_kq[buf]);
+        tma_load_3d(dst + 16384, &p.tm_k, 64, h, t0, &bar_kq[buf]);
+        tma_load_3d(dst + 16384 + 8192, &p.tm_q, 64, h, t0, &bar_kq[buf]);
+        atomicMax(&cnt[0], c + 1);
     };
-    auto issue_v = [&](int pos) {   // thread 0
+    auto issue_v = [&](int c, int pos) {
         proxy_fence();
         mbar_arrive_expect_tx(bar_v, 2u * 8192u);
         const int t0 = (int)(tok_begin + pos);
         tma_load_3d(smem + OFF_V, &p.tm_v, 0, h, t0, bar_v);
         tma_load_3d(smem + OFF_V + 8192, &p.tm_v, 64, h, t0, bar_v);
+        atomicMax(&cnt[1], c + 1);
     };
-    // 64-token window from pos, cut at the next checkpoint and at the end of the job
-    auto next_window = [&](int pos, int& ck) -> Pos {
-        int end = pos + C < len ? pos + C : len;
-        while (ck < ck_end && p.ckpts[ck].pos <= pos) ++ck;
-        if (ck < ck_end && p.ckpts[ck].pos < end) end = p.ckpts[ck].pos;
-        return Pos{pos, end - pos};
-    };
-    // bounded wait by every thread; the block agrees on the outcome
-    auto block_wait = [&](uint64_t* b, uint32_t parity) -> bool {
-        bool w = mbar_try_wait(b, parity);
-        if (!w) {
-            const uint64_t t0 = global_ns();
-            while (!(w = mbar_try_wait(b, parity)))
-                if (global_ns() - t0 > limit) break;
+
+    if (len == 0) {
+        // empty range: the final state is the initial one
+        if (warp < 4 && job.s_final) {
+            for (int c0 = 0; c0 < D; c0 += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (job.s0) x = __ldg(reinterpret_cast<const float4*>(job.s0 + head_state + (size_t)row * D + c0));
+                *reinterpret_cast<float4*>(job.s_final + head_state + (size_t)row * D + c0) = x;
+            }
         }
-        return __syncthreads_and(w) != 0;
-    };
-    // gates of a window, held by warp 0: tokens lane and lane + 32 (alpha = 1, beta = 0 past it)
-    auto load_gates = [&](Pos c, float& a0, float& a1, float& b0, float& b1) {
-        a0 = a1 = 1.f;
-        b0 = b1 = 0.f;
-        const size_t gbase = (size_t)(tok_begin + c.begin) * (size_t)H + (size_t)h;
-        if (lane < c.len) {
-            a0 = __ldg(p.alpha + gbase + (size_t)lane * H);
-            b0 = __ldg(p.beta + gbase + (size_t)lane * H);
-        }
-        if (lane + 32 < c.len) {
-            a1 = __ldg(p.alpha + gbase + (size_t)(lane + 32) * H);
-            b1 = __ldg(p.beta + gbase + (size_t)(lane + 32) * H);
-        }
-    };
-    auto prefix = [&](float a0, float a1, float& g0, float& g1) {   // warp 0: inclusive products
-        g0 = a0;
-        g1 = a1;
+    } else if (warp < 4) {
+        // ============================ chain group ============================
+        auto split_state = [&](const Ring& R) {
+            // St -> bf16 hi/lo pairs (the A operand); a single small-alpha token then scales St
+            const bool single = R.single != 0;
+            const float f = R.prescale;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                float v[32];
+                tmem_ld32(trow + T_S + 32 * cb, v);
+                uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float x0 = __shfl_up_sync(0xffffffffu, g0, off);
-            const float x1 = __shfl_up_sync(0xffffffffu, g1, off);
-            if (lane >= off) {
-                g0 *= x0;
-                g1 *= x1;
+                for (int e = 0; e < 16; ++e) split_pair(v[2 * e], v[2 * e + 1], hw[e], lw[e]);
+                tmem_st16(trow + T_SH + 16 * cb, hw);
+                tmem_st16(trow + T_SL + 16 * cb, lw);
+                if (single) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= f;
+                    tmem_st32(trow + T_S + 32 * cb, v);
+                }
+            }
+            tmem_st_wait();
+        };
+        auto fold_state = [&](const Ring& R) {
+            float* d1 = R.dump_slot >= 0 ? p.ckpt_states + (size_t)R.dump_slot * (size_t)H * D * D + head_state : nullptr;
+            float* d2 = (R.last && job.s_final) ? job.s_final + head_state : nullptr;
+            const float f = R.sigma_after;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                float v[32];
+                tmem_ld32(trow + T_S + 32 * cb, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= f;
+                tmem_st32(trow + T_S + 32 * cb, v);
+                if (d1) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(d1 + (size_t)row * D + 32 * cb + i) =
+                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                }
+                if (d2) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(d2 + (size_t)row * D + 32 * cb + i) =
+                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                }
+            }
+            tmem_st_wait();
+        };
+        auto readout = [&](const Ring& R, float u0) {
+            // every schedule field into registers first: the output stores may alias shared memory
+            const int n = R.n;
+            const bool single = R.single != 0;
+            const float qk0 = R.qk0;
+            const size_t tstride = (size_t)H * D;
+            OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)(o_row0 + R.begin) * tstride + (size_t)h * D + row;
+#pragma unroll 1
+            for (int cb = 0; cb < 2 && 32 * cb < n; ++cb) {
+                float v[32], rs[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(&R.rs[32 * cb + i]);
+                    rs[i] = x.x;
+                    rs[i + 1] = x.y;
+                    rs[i + 2] = x.z;
+                    rs[i + 3] = x.w;
+                }
+                tmem_ld32(trow + T_O + 32 * cb, v);
+                if (cb == 0 && single) v[0] = fmaf(qk0, u0, rs[0] * v[0]);
+                else if (cb == 0) v[0] *= rs[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) v[j] *= rs[j];
+                if (cb == 1) v[0] *= rs[0];
+                const int m = n - 32 * cb;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (j < m) {
+                        OutT* op = ob + (size_t)(32 * cb + j) * tstride;
+                        if constexpr (OUT_BF16)
+                            *op = __float2bfloat16_rn(v[j]);
+                        else
+                            *op = v[j];
+                    }
+                }
+            }
+        };
+
+        // St = S_0 (sigma = 1)
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (job.s0) x = __ldg(reinterpret_cast<const float4*>(job.s0 + head_state + (size_t)row * D + 32 * cb + i));
+                v[i] = x.x;
+                v[i + 1] = x.y;
+                v[i + 2] = x.z;
+                v[i + 3] = x.w;
+            }
+            tmem_st32(trow + T_S + 32 * cb, v);
+        }
+        tmem_st_wait();
+        bool ok = group_wait(&bar_ring[0], 0, tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit);
+        if (ok) {
+            split_state(ring[0]);
+            tc_fence_before();
+            mbar_arrive(bar_split);
+            float u0_prev = 0.f;
+            for (int j = 0;; ++j) {
+                const Ring& R = ring[j % kRing];
+                // ---- readout of the previous chunk while U^T of this one is computed ----
+                if (rd && j > 0) {
+                    if (!group_wait(bar_o, (uint32_t)((j - 1) & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
+                    tc_fence_after();
+                    readout(ring[(j - 1) % kRing], u0_prev);
+                    tc_fence_before();
+                    mbar_arrive(bar_ofree);
+                }
+                // ---- U'' = c_t U as bf16 hi/lo (K-major A operand [d_v][t]) ----
+                if (!group_wait(bar_uo, (uint32_t)(j & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
+                tc_fence_after();
+                float u0 = 0.f;
+#pragma unroll 1
+                for (int cb = 0; cb < 2; ++cb) {
+                    float v[32], c[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(&R.c[32 * cb + i]);
+                        c[i] = x.x;
+                        c[i + 1] = x.y;
+                        c[i + 2] = x.z;
+                        c[i + 3] = x.w;
+                    }
+                    tmem_ld32(trow + T_U + 32 * cb, v);
+                    if (cb == 0) u0 = v[0];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= c[i];
+                    st_split32(smem + OFF_UH, smem + OFF_UL, row, 32 * cb, v);
+                }
+                proxy_fence();
+                tc_fence_before();
+                mbar_arrive(bar_ufree);
+                // ---- after St += U''^T K: checkpoint / end / small scale -> fold sigma into St ----
+                if (!group_wait(bar_st, (uint32_t)(j & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
+                tc_fence_after();
+                const bool fold = R.fold != 0, last = R.last != 0;
+                if (fold) fold_state(R);
+                u0_prev = u0;
+                if (last) {
+                    if (rd) {
+                        if (!group_wait(bar_o, (uint32_t)(j & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
+                        tc_fence_after();
+                        readout(R, u0_prev);
+                    }
+                    break;
+                }
+                // ---- next chunk: its K/Q two chunks ahead into the buffer just freed, then split St ----
+                const int jn = j + 1;
+                if (!group_wait(&bar_ring[jn % kRing], (uint32_t)((jn / kRing) & 1), tid == 0, BAR_CHAIN, NCHAIN,
+                                abort_flag, limit))
+                    break;
+                const Ring& Rn = ring[jn % kRing];
+                if (tid == 0 && Rn.next_len > 0 && allowed(j + 2)) issue_kq(j + 2, Rn.next_begin);
+                split_state(Rn);
+                tc_fence_before();
+                mbar_arrive(bar_split);
             }
         }
-        g1 *= __shfl_sync(0xffffffffu, g0, 31);
-    };
-
-    bool ok = true;
-    bool mma_pending = false;
-    int ck_sched = job.ck_begin;   // schedule cursor (advanced by warp 0 only)
-    int ck_dump = job.ck_begin;
-    Pos cur = next_window(0, ck_sched);
-    int chunk_no = 0, kq_issued = 0, v_issued = 0;
-    uint32_t mma_phase = 0;
-    float sigma = 1.f;   // S = sigma St (the same in every thread)
-    float ga0 = 1.f, ga1 = 1.f, gb0 = 0.f, gb1 = 0.f;
-    const bool stall_on = p.stall_after >= 0;   // testing hook: stop issuing copies after stall_after chunks
-    if (len > 0) {
-        if (!stall_on || p.stall_after > 0) {
-            if (tid == 0) {
-                issue_kq(0, 0);
-                issue_v(0);
+    } else if (warp < 12) {
+        // ============================ prep group ============================
+        const int ptid = tid - NCHAIN;           // 0..255
+        const int pw = warp - 4;                 // 0..7
+        const int half = pw >> 2;                // column half of G / W handled by this warp
+        const bool leader = ptid == 0;
+        // gate warp (pw == 3) state: schedule cursors, running scale, the next window's gates
+        int g_ck_sched = job.ck_begin, g_ck_dump = job.ck_begin;
+        float g_sigma = 1.f;
+        Pos g_win{0, 0};
+        float ga0 = 1.f, ga1 = 1.f, gb0 = 0.f, gb1 = 0.f;
+        auto next_window = [&](int pos, int& ck) -> Pos {
+            int end = pos + C < len ? pos + C : len;
+            while (ck < ck_end && p.ckpts[ck].pos <= pos) ++ck;
+            if (ck < ck_end && p.ckpts[ck].pos < end) end = p.ckpts[ck].pos;
+            return Pos{pos, end - pos};
+        };
+        auto load_gates = [&](Pos c) {
+            ga0 = ga1 = 1.f;
+            gb0 = gb1 = 0.f;
+            const size_t gbase = (size_t)(tok_begin + c.begin) * (size_t)H + (size_t)h;
+            if (lane < c.len) {
+                ga0 = __ldg(p.alpha + gbase + (size_t)lane * H);
+                gb0 = __ldg(p.beta + gbase + (size_t)lane * H);
             }
-            kq_issued = 1;
-            v_issued = 1;
-        }
-        if (warp == 0) load_gates(cur, ga0, ga1, gb0, gb1);
-    }
-
-    auto mma_wait = [&]() -> bool {
-        const bool r = block_wait(bar_mma, mma_phase & 1);
-        ++mma_phase;
-        tc_fence_after();
-        return r;
-    };
-
-    while (len > 0 && cur.begin < len) {
-        const int buf = chunk_no & 1;
-        const uint32_t inKQ = sbase + OFF_IN + buf * 32768;
-        const uint32_t inV = sbase + OFF_V;
-        const float sigma0 = sigma;
-
-        // ---- gates: gamma, the cut where gamma < 2^-32, per-token scalars; next window's gates ----
-        if (warp == 0) {
+            if (lane + 32 < c.len) {
+                ga1 = __ldg(p.alpha + gbase + (size_t)(lane + 32) * H);
+                gb1 = __ldg(p.beta + gbase + (size_t)(lane + 32) * H);
+            }
+        };
+        auto prefix = [&](float a0, float a1, float& g0, float& g1) {   // inclusive products over the warp
+            g0 = a0;
+            g1 = a1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float x0 = __shfl_up_sync(0xffffffffu, g0, off);
+                const float x1 = __shfl_up_sync(0xffffffffu, g1, off);
+                if (lane >= off) {
+                    g0 *= x0;
+                    g1 *= x1;
+                }
+            }
+            g1 *= __shfl_sync(0xffffffffu, g0, 31);
+        };
+        // schedule and scalars of chunk jj (window g_win), published in ring[jj % kRing]
+        auto compute_chunk = [&](int jj) {
             float a0 = ga0, a1 = ga1, b0 = gb0, b1 = gb1;
             float g0, g1;
             prefix(a0, a1, g0, g1);
             const unsigned m0 = __ballot_sync(0xffffffffu, g0 < kGammaFloor);
             const unsigned m1 = __ballot_sync(0xffffffffu, g1 < kGammaFloor);
             const int first = m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : C);
-            int n = cur.len;
+            int n = g_win.len;
             if (first < n) {
                 n = first > 0 ? first : 1;
                 if (lane >= n) {
@@ -368,405 +587,427 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 }
                 prefix(a0, a1, g0, g1);
             }
-            const bool single = n == 1 && __shfl_sync(0xffffffffu, g0, 0) < kGammaFloor;
-            const Pos nx = (cur.begin + n < len) ? next_window(cur.begin + n, ck_sched) : Pos{len, 0};
-            if (nx.len > 0) load_gates(nx, ga0, ga1, gb0, gb1);
-            sc_g[lane] = g0;
-            sc_g[lane + 32] = g1;
-            sc_ginv[lane] = __frcp_rn(g0);
-            sc_ginv[lane + 32] = __frcp_rn(g1);
-            sc_bg[lane] = b0 * g0;
-            sc_bg[lane + 32] = b1 * g1;
-            sc_b[lane] = b0;
-            sc_b[lane + 32] = b1;
-            sc_c[lane] = lane < n ? (single ? 1.f : __frcp_rn(sigma0 * g0)) : 0.f;
-            sc_c[lane + 32] = lane + 32 < n ? __frcp_rn(sigma0 * g1) : 0.f;
-            sc_p[lane] = single ? 1.f : sigma0 * g0;
-            sc_p[lane + 32] = sigma0 * g1;
+            const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
+            const float glast = __shfl_sync(0xffffffffu, n > 32 ? g1 : g0, (n - 1) & 31);
+            const bool single = n == 1 && gfirst < kGammaFloor;
+            const int chunk_end = g_win.begin + n;
+            while (g_ck_dump < ck_end && p.ckpts[g_ck_dump].pos < chunk_end) ++g_ck_dump;
+            const bool dump = g_ck_dump < ck_end && p.ckpts[g_ck_dump].pos == chunk_end;
+            const bool last = chunk_end >= len;
+            const float sigma0 = g_sigma;
+            const float s_after = single ? 1.f : sigma0 * glast;
+            const bool fold = dump || last || s_after < kSigmaFloor;
+            const Pos nx = last ? Pos{len, 0} : next_window(chunk_end, g_ck_sched);
+            float* ps = psc + (jj & 1) * 4 * C;
+            ps[lane] = g0;
+            ps[lane + 32] = g1;
+            ps[C + lane] = __frcp_rn(g0);
+            ps[C + lane + 32] = __frcp_rn(g1);
+            ps[2 * C + lane] = b0 * g0;
+            ps[2 * C + lane + 32] = b1 * g1;
+            ps[3 * C + lane] = b0;
+            ps[3 * C + lane + 32] = b1;
+            Ring& R = ring[jj % kRing];
+            R.rs[lane] = single ? (lane == 0 ? sigma0 * g0 : 0.f) : sigma0 * g0;
+            R.rs[lane + 32] = single ? 0.f : sigma0 * g1;
+            R.c[lane] = lane < n ? (single ? 1.f : __frcp_rn(sigma0 * g0)) : 0.f;
+            R.c[lane + 32] = lane + 32 < n ? __frcp_rn(sigma0 * g1) : 0.f;
             if (lane == 0) {
-                sh_sched[0] = n;
-                sh_sched[1] = single ? 1 : 0;
-                sh_sched[2] = nx.begin;
-                sh_sched[3] = nx.len;
+                R.begin = g_win.begin;
+                R.n = n;
+                R.single = single ? 1 : 0;
+                R.fold = fold ? 1 : 0;
+                R.dump_slot = dump ? p.ckpts[g_ck_dump].slot : -1;
+                R.last = last ? 1 : 0;
+                R.next_begin = nx.begin;
+                R.next_len = nx.len;
+                R.sigma0 = sigma0;
+                R.sigma_after = s_after;
+                R.prescale = single ? sigma0 * gfirst : 1.f;
+                R.qk0 = 0.f;
             }
+            g_sigma = fold ? 1.f : s_after;
+            g_win = nx;
+            if (nx.len > 0) load_gates(nx);
+            mbar_arrive(&bar_ring[jj % kRing]);
+        };
+
+        if (pw == 3) {
+            g_win = next_window(0, g_ck_sched);
+            load_gates(g_win);
+            if (lane == 0 && allowed(0)) {
+                issue_kq(0, 0);
+                issue_v(0, 0);
+            }
+            compute_chunk(0);
+            if (lane == 0 && ring[0].next_len > 0 && allowed(1)) issue_kq(1, ring[0].next_begin);
         }
-        // ---- wait for this chunk's K, Q, V ----
-        if (!block_wait(&bar_in[buf], (uint32_t)((chunk_no >> 1) & 1))) { ok = false; break; }
-        if (!block_wait(bar_v, (uint32_t)(chunk_no & 1))) { ok = false; break; }
-        const int clen = sh_sched[0];
-        const bool single = sh_sched[1] != 0;
-        const Pos nxt = Pos{sh_sched[2], sh_sched[3]};
-        // zero the tile rows past the chunk (whole 128-byte rows: the swizzle stays within a row)
-        if (clen < C) {
-            const int nz = C - clen;
-            for (int i = tid; i < 6 * nz * 8; i += NTHREADS) {
-                const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;   // part 0-3: [K;Q], 4-5: V
-                unsigned char* base = part < 4 ? smem + OFF_IN + buf * 32768 + (part >> 1) * 16384 + (part & 1) * 8192
-                                               : smem + OFF_V + (part - 4) * 8192;
-                *reinterpret_cast<uint4*>(base + (clen + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
+        group_sync(BAR_PREP, NPREP);
+
+        for (int j = 0;; ++j) {
+            const Ring& R = ring[j % kRing];
+            const int n = R.n;
+            const bool single = R.single != 0;
+            const bool last = R.last != 0;
+            const float* ps = psc + (j & 1) * 4 * C;
+
+            // ---- this chunk's K, Q, V; zero the tile rows past the chunk ----
+            if (!group_wait(&bar_kq[j & 1], (uint32_t)((j >> 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit) ||
+                !group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
+                break;
+            if (n < C) {
+                const int nz = C - n;
+                for (int i = ptid; i < 6 * nz * 8; i += NPREP) {
+                    const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;   // part 0-3: [K;Q], 4-5: V
+                    unsigned char* base = part < 4 ? smem + OFF_KQ + (j & 1) * 32768 + (part >> 1) * 16384 + (part & 1) * 8192
+                                                   : smem + OFF_V + (part - 4) * 8192;
+                    *reinterpret_cast<uint4*>(base + (n + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                proxy_fence();
+            }
+            tc_fence_before();
+            group_sync(BAR_PREP, NPREP);
+            if (leader) mbar_arrive(bar_gin);
+
+            // ---- G = [K; Q] K^T; then L (fp32, zero on and above the diagonal) ----
+            if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+            tc_fence_after();
+            if (lq < 2) {
+                const int t = row, s0 = 32 * half;
+                float gi[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(ps + C + s0 + i);
+                    gi[i] = x.x;
+                    gi[i + 1] = x.y;
+                    gi[i + 2] = x.z;
+                    gi[i + 3] = x.w;
+                }
+                const float f = ps[2 * C + t];
+                float v[32];
+                tmem_ld32(trow + T_G + 32 * half, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = (s0 + i < t) ? f * gi[i] * v[i] : 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<float4*>(Lf + t * kLdF + s0 + 4 * q4) =
+                        make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                // the 16x16 diagonal block of row t, if it lies in this half
+                if ((t >> 5) == half) {
+                    const int b0 = (t & 16);   // 0 or 16 within the half
+                    float* dst = Ld + (t >> 4) * 16 * 17 + (t & 15) * 17;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[i] = (b0 == 0) ? v[i] : v[16 + i];
+                }
+            } else if (pw == 3 && !last) {
+                compute_chunk(j + 1);   // the gate warp runs one chunk ahead
+            }
+            group_sync(BAR_PREP, NPREP);
+
+            // ---- T = (I + L)^-1 in place over Lf: 16x16 diagonal inverses, then a two-level merge ----
+            if (pw < 4 && lane < 16) {
+                const int b = pw, jc = lane;
+                const float* Lb = Ld + b * 16 * 17;
+                float x[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    float vv = (t == jc) ? 1.f : 0.f;
+#pragma unroll
+                    for (int s2 = 0; s2 < t; ++s2) vv = fmaf(-Lb[t * 17 + s2], x[s2], vv);
+                    x[t] = vv;
+                }
+#pragma unroll
+                for (int t = 0; t < 16; ++t) Lf[(16 * b + t) * kLdF + 16 * b + jc] = x[t];
+            }
+            group_sync(BAR_PREP, NPREP);
+            {   // T_10 = -T_11 L_10 T_00 (threads 0-127) and T_32 = -T_33 L_32 T_22 (threads 128-255)
+                const int grp = ptid >> 7, tg = ptid & 127;
+                const int jb = 2 * grp, ib = jb + 1;
+                const int r = tg >> 3, c = 2 * (tg & 7);
+                float* Y = Yb + grp * 16 * 17;
+                float y0 = 0.f, y1 = 0.f;
+                const float* Lr = Lf + (16 * ib + r) * kLdF + 16 * jb;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float l = Lr[m];
+                    const float2 tv = *reinterpret_cast<const float2*>(Lf + (16 * jb + m) * kLdF + 16 * jb + c);
+                    y0 = fmaf(l, tv.x, y0);
+                    y1 = fmaf(l, tv.y, y1);
+                }
+                Y[r * 17 + c] = y0;
+                Y[r * 17 + c + 1] = y1;
+                group_sync(BAR_PREP_A + grp, 128);
+                float x0 = 0.f, x1 = 0.f;
+                const float* Ti = Lf + (16 * ib + r) * kLdF + 16 * ib;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float tv = Ti[m];
+                    x0 = fmaf(tv, Y[m * 17 + c], x0);
+                    x1 = fmaf(tv, Y[m * 17 + c + 1], x1);
+                }
+                Lf[(16 * ib + r) * kLdF + 16 * jb + c] = -x0;
+                Lf[(16 * ib + r) * kLdF + 16 * jb + c + 1] = -x1;
+            }
+            group_sync(BAR_PREP, NPREP);
+            {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block
+                const int r = ptid >> 3, c = 4 * (ptid & 7);
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                const float* Lr = Lf + (32 + r) * kLdF;
+#pragma unroll 8
+                for (int m = 0; m < 32; ++m) {
+                    const float l = Lr[m];
+                    const float4 tv = *reinterpret_cast<const float4*>(Lf + m * kLdF + c);
+                    y[0] = fmaf(l, tv.x, y[0]);
+                    y[1] = fmaf(l, tv.y, y[1]);
+                    y[2] = fmaf(l, tv.z, y[2]);
+                    y[3] = fmaf(l, tv.w, y[3]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Yb[r * 33 + c + e] = y[e];
+                group_sync(BAR_PREP, NPREP);
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                const float* Tr = Lf + (32 + r) * kLdF + 32;
+#pragma unroll 8
+                for (int m = 0; m < 32; ++m) {
+                    const float tv = Tr[m];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) x[e] = fmaf(tv, Yb[m * 33 + c + e], x[e]);
+                }
+                *reinterpret_cast<float4*>(Lf + (32 + r) * kLdF + c) = make_float4(-x[0], -x[1], -x[2], -x[3]);
+            }
+            group_sync(BAR_PREP, NPREP);
+            // ---- T1 = T diag(beta gamma), T2 = T diag(beta) as bf16 hi/lo, K-major [t][s] ----
+            {
+                const int t = ptid >> 2, s0 = 16 * (ptid & 3);
+                float tv[16], bg[16], bb[16];
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + i);
+                    const float4 y = *reinterpret_cast<const float4*>(ps + 2 * C + s0 + i);
+                    const float4 z = *reinterpret_cast<const float4*>(ps + 3 * C + s0 + i);
+                    tv[i] = x.x; tv[i + 1] = x.y; tv[i + 2] = x.z; tv[i + 3] = x.w;
+                    bg[i] = y.x; bg[i + 1] = y.y; bg[i + 2] = y.z; bg[i + 3] = y.w;
+                    bb[i] = z.x; bb[i + 1] = z.y; bb[i + 2] = z.z; bb[i + 3] = z.w;
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t ah[4], al[4], bh[4], bl[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 8 * q + 2 * e;
+                        split_pair(tv[i] * bg[i], tv[i + 1] * bg[i + 1], ah[e], al[e]);
+                        split_pair(tv[i] * bb[i], tv[i + 1] * bb[i + 1], bh[e], bl[e]);
+                    }
+                    const uint32_t o = sw128(t, s0 + 8 * q);
+                    *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+                    *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(al[0], al[1], al[2], al[3]);
+                    *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+                    *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+                }
             }
             proxy_fence();
-            __syncthreads();
-        }
+            group_sync(BAR_PREP, NPREP);
+            if (leader) mbar_arrive(bar_wuin);
 
-        // ---- G = [K; Q] K^T ----
-        const bool issue_next_kq = nxt.len > 0 && kq_issued == chunk_no + 1 && (!stall_on || kq_issued < p.stall_after);
-        if (tid == 0) {
+            // ---- W^T = K^T T1^T, U~^T = V^T T2^T; then -sigma_0 W^T as the MN-major B operand ----
+            if (!group_wait(bar_wu, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             tc_fence_after();
-            const uint32_t id = idesc(64, false, false);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id, kk > 0);
-            }
-            umma_commit(bar_mma);
-            // the other K/Q buffer was last read by the previous chunk's MMAs, which have completed
-            if (issue_next_kq) issue_kq(buf ^ 1, nxt.begin);
-        }
-        if (issue_next_kq) ++kq_issued;
-        mma_pending = true;
-        if (!mma_wait()) { ok = false; break; }
-        mma_pending = false;
-
-        // ---- L (fp32, zero on and above the diagonal) and P'' = pscale_t mask(q_t.k_s) (bf16 hi/lo) ----
-        {
-            float v[32];
-            tmem_ld32(trow + T_G + 32 * half, v);
-            const int s0 = 32 * half;
-            if (row < 64) {
-                const int t = row;
-                const float f = sc_bg[t];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int s = s0 + j;
-                    const float l = s < t ? f * sc_ginv[s] * v[j] : 0.f;
-                    Lf[t * kLdF + s] = l;
-                    if ((s >> 4) == (t >> 4)) Ld[(t >> 4) * 16 * 17 + (t & 15) * 17 + (s & 15)] = l;
-                }
-            } else if (rd) {
-                const int t = row - 64;
-                const float ps = sc_p[t];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = (s0 + j <= t) ? ps * v[j] : 0.f;
-                st_split32(smem + OFF_PH, smem + OFF_PL, t, s0, v);
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- T = (I + L)^-1 in place over Lf: 16x16 diagonal inverses, then a two-level merge ----
-        if (warp < 4 && lane < 16) {
-            const int b = warp, j = lane;
-            const float* Lb = Ld + b * 16 * 17;
-            float x[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                float vv = (t == j) ? 1.f : 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < t; ++s2) vv = fmaf(-Lb[t * 17 + s2], x[s2], vv);
-                x[t] = vv;
-            }
-#pragma unroll
-            for (int t = 0; t < 16; ++t) Lf[(16 * b + t) * kLdF + 16 * b + j] = x[t];
-        }
-        __syncthreads();
-        {   // T_10 = -T_11 L_10 T_00 (threads 0-127) and T_32 = -T_33 L_32 T_22 (threads 128-255)
-            const int grp = tid >> 7, tg = tid & 127;
-            const int jb = 2 * grp, ib = jb + 1;
-            const int r = tg >> 3, c = 2 * (tg & 7);
-            float* Y = Yb + grp * 16 * 17;
-            float y0 = 0.f, y1 = 0.f;
-            const float* Lr = Lf + (16 * ib + r) * kLdF + 16 * jb;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float l = Lr[m];
-                const float2 tv = *reinterpret_cast<const float2*>(Lf + (16 * jb + m) * kLdF + 16 * jb + c);
-                y0 = fmaf(l, tv.x, y0);
-                y1 = fmaf(l, tv.y, y1);
-            }
-            Y[r * 17 + c] = y0;
-            Y[r * 17 + c + 1] = y1;
-            asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory");
-            float x0 = 0.f, x1 = 0.f;
-            const float* Ti = Lf + (16 * ib + r) * kLdF + 16 * ib;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float tv = Ti[m];
-                x0 = fmaf(tv, Y[m * 17 + c], x0);
-                x1 = fmaf(tv, Y[m * 17 + c + 1], x1);
-            }
-            Lf[(16 * ib + r) * kLdF + 16 * jb + c] = -x0;
-            Lf[(16 * ib + r) * kLdF + 16 * jb + c + 1] = -x1;
-        }
-        __syncthreads();
-        {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block
-            const int r = tid >> 3, c = 4 * (tid & 7);
-            float y[4] = {0.f, 0.f, 0.f, 0.f};
-            const float* Lr = Lf + (32 + r) * kLdF;
-#pragma unroll 8
-            for (int m = 0; m < 32; ++m) {
-                const float l = Lr[m];
-                const float4 tv = *reinterpret_cast<const float4*>(Lf + m * kLdF + c);
-                y[0] = fmaf(l, tv.x, y[0]);
-                y[1] = fmaf(l, tv.y, y[1]);
-                y[2] = fmaf(l, tv.z, y[2]);
-                y[3] = fmaf(l, tv.w, y[3]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Yb[r * 33 + c + e] = y[e];
-            __syncthreads();
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-            const float* Tr = Lf + (32 + r) * kLdF + 32;
-#pragma unroll 8
-            for (int m = 0; m < 32; ++m) {
-                const float tv = Tr[m];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x[e] = fmaf(tv, Yb[m * 33 + c + e], x[e]);
-            }
-            *reinterpret_cast<float4*>(Lf + (32 + r) * kLdF + c) = make_float4(-x[0], -x[1], -x[2], -x[3]);
-        }
-        __syncthreads();
-        // ---- T1 = T diag(beta gamma), T2 = T diag(beta) as bf16 hi/lo, K-major [t][s] ----
-        {
-            const int t = tid >> 2, s0 = 16 * (tid & 3);
-            float x1[16], x2[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float tv = Lf[t * kLdF + s0 + j];
-                x1[j] = tv * sc_bg[s0 + j];
-                x2[j] = tv * sc_b[s0 + j];
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                uint32_t ah[4], al[4], bh[4], bl[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    split_pair(x1[8 * q + 2 * e], x1[8 * q + 2 * e + 1], ah[e], al[e]);
-                    split_pair(x2[8 * q + 2 * e], x2[8 * q + 2 * e + 1], bh[e], bl[e]);
-                }
-                const uint32_t o = sw128(t, s0 + 8 * q);
-                *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(al[0], al[1], al[2], al[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-                *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-            }
-        }
-        proxy_fence();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- W^T = K^T T1^T, U~^T = V^T T2^T (into the U^T accumulator) ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc(64, true, false);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
-                const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
-                umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id, ks > 0);
-                umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id, 1);
-                umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id, ks > 0);
-                umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id, 1);
-            }
-            umma_commit(bar_mma);
-        }
-        mma_pending = true;
-        // ---- meanwhile: S_0 = sigma_0 St as bf16 hi/lo pairs in TMEM (the A operand); a single
-        //      small-alpha token first takes St to alpha_1 S_0 ----
-        {
-            const float pre = sigma0 * sc_g[0];
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                const int c0 = 64 * half + 32 * cb;
+            if (leader && !last && allowed(j + 1)) issue_v(j + 1, R.next_begin);   // the V buffer is free again
+            {
+                const float f = -R.sigma0;
                 float v[32];
-                tmem_ld32(trow + T_S + c0, v);
-                uint32_t hw[16], lw[16];
+                tmem_ld32(trow + T_W + 32 * half, v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) split_pair(sigma0 * v[2 * e], sigma0 * v[2 * e + 1], hw[e], lw[e]);
-                tmem_st16(trow + T_SH + c0 / 2, hw);
-                tmem_st16(trow + T_SL + c0 / 2, lw);
-                if (single) {
+                for (int i = 0; i < 32; ++i) v[i] *= f;
+                st_split32(smem + OFF_WH, smem + OFF_WL, row, 32 * half, v);
+            }
+            proxy_fence();
+            tc_fence_before();
+            mbar_arrive(bar_wready);
+
+            // ---- P = mask(q_t . k_s), once the chain's previous U''^T P^T is done ----
+            if (rd) {
+                if (j > 0 && !group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
+                    break;
+                if (lq >= 2) {
+                    float v[32];
+                    tmem_ld32(trow + T_G + 32 * half, v);
+                    const int t = row - 64, s0 = 32 * half;
+                    if (single && t == 0 && half == 0) ring[j % kRing].qk0 = v[0];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] *= pre;
-                    tmem_st32(trow + T_S + c0, v);
+                    for (int i = 0; i < 32; ++i) v[i] = (!single && s0 + i <= t) ? v[i] : 0.f;
+                    st_split32(smem + OFF_PH, smem + OFF_PL, t, s0, v);
+                }
+                proxy_fence();
+                tc_fence_before();
+                mbar_arrive(bar_pready);
+            }
+            if (last) break;
+        }
+    } else if (lane == 0) {
+        // ============================ MMA issue (warp 12, one lane) ============================
+        // Two streams, each in its own order: chain U_j, O1_j, St_j, O2_j and prep G_j, WU_j.  An item
+        // is issued once the mbarriers of its operands have fired; a stream ends after its last chunk.
+        int jc = 0, sc = 0, jp = 0, sp = 0;
+        bool chain_done = false, prep_done = false;
+        uint64_t t_last = global_ns();
+        const uint32_t id64 = idesc(64, false, false), id64b = idesc(64, false, true), id64a = idesc(64, true, false);
+        const uint32_t id128b = idesc(128, false, true);
+        while (!(chain_done && prep_done)) {
+            bool progressed = false;
+            if (!chain_done) {
+                const Ring& R = ring[jc % kRing];
+                const uint32_t inKQ = sbase + OFF_KQ + (jc & 1) * 32768;
+                if (sc == 0) {
+                    if (mbar_test(bar_split, jc & 1) && mbar_test(bar_wready, jc & 1)) {
+                        tc_fence_after();
+                        // U^T += St (-sigma_0 W)^T  (St from TMEM as bf16 hi/lo pairs)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bwh = sdesc(sbase + OFF_WH + kk * 2048, 16384, 1024);
+                            const uint64_t bwl = sdesc(sbase + OFF_WL + kk * 2048, 16384, 1024);
+                            const uint32_t ah = tbase + T_SH + 8 * kk, al = tbase + T_SL + 8 * kk;
+                            umma_ts(tbase + T_U, ah, bwh, id64b, 1);
+                            umma_ts(tbase + T_U, ah, bwl, id64b, 1);
+                            umma_ts(tbase + T_U, al, bwh, id64b, 1);
+                        }
+                        umma_commit(bar_uo);
+                        ++cnt[4];
+                        sc = rd ? 1 : 2;
+                        progressed = true;
+                    }
+                }
+                if (sc == 1) {
+                    if (jc == 0 || mbar_test(bar_ofree, (jc - 1) & 1)) {
+                        tc_fence_after();
+                        // O^T = St Q^T
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bq = sdesc(inKQ + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                            umma_ts(tbase + T_O, tbase + T_SH + 8 * kk, bq, id64, kk > 0);
+                            umma_ts(tbase + T_O, tbase + T_SL + 8 * kk, bq, id64, 1);
+                        }
+                        sc = 2;
+                        progressed = true;
+                    }
+                }
+                if (sc == 2) {
+                    if (mbar_test(bar_ufree, jc & 1)) {
+                        tc_fence_after();
+                        // St += U''^T K
+#pragma unroll
+                        for (int kt = 0; kt < 4; ++kt) {
+                            const uint64_t auh = sdesc(sbase + OFF_UH + kt * 32, 16, 1024);
+                            const uint64_t aul = sdesc(sbase + OFF_UL + kt * 32, 16, 1024);
+                            const uint64_t bk = sdesc(inKQ + kt * 2048, 16384, 1024);   // K: MN-major over d_k
+                            umma_ss(tbase + T_S, auh, bk, id128b, 1);
+                            umma_ss(tbase + T_S, aul, bk, id128b, 1);
+                        }
+                        umma_commit(bar_st);
+                        ++cnt[5];
+                        sc = rd ? 3 : 4;
+                        progressed = true;
+                    }
+                }
+                if (sc == 3) {
+                    if (mbar_test(bar_pready, jc & 1)) {
+                        tc_fence_after();
+                        if (!R.single) {
+                            // O^T += U''^T P^T
+#pragma unroll
+                            for (int kt = 0; kt < 4; ++kt) {
+                                const uint64_t auh = sdesc(sbase + OFF_UH + kt * 32, 16, 1024);
+                                const uint64_t aul = sdesc(sbase + OFF_UL + kt * 32, 16, 1024);
+                                const uint64_t bph = sdesc(sbase + OFF_PH + kt * 32, 16, 1024);
+                                const uint64_t bpl = sdesc(sbase + OFF_PL + kt * 32, 16, 1024);
+                                umma_ss(tbase + T_O, auh, bph, id64, 1);
+                                umma_ss(tbase + T_O, auh, bpl, id64, 1);
+                                umma_ss(tbase + T_O, aul, bph, id64, 1);
+                            }
+                        }
+                        umma_commit(bar_o);
+                        ++cnt[6];
+                        sc = 4;
+                        progressed = true;
+                    }
+                }
+                if (sc == 4) {
+                    if (R.last) chain_done = true;
+                    else {
+                        ++jc;
+                        sc = 0;
+                    }
                 }
             }
-            tmem_st_wait();
-        }
-        if (!mma_wait()) { ok = false; break; }
-        mma_pending = false;
-        // the V buffer is free again: fetch the next chunk's V
-        const bool issue_next_v = nxt.len > 0 && v_issued == chunk_no + 1 && (!stall_on || v_issued < p.stall_after);
-        if (issue_next_v && tid == 0) issue_v(nxt.begin);
-        if (issue_next_v) ++v_issued;
-        // ---- -W^T as the MN-major B operand [d_k][t] ----
-        {
-            float v[32];
-            tmem_ld32(trow + T_W + 32 * half, v);
+            if (!prep_done) {
+                const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
+                if (sp == 0) {
+                    if (mbar_test(bar_gin, jp & 1)) {
+                        tc_fence_after();
+                        // G = [K; Q] K^T
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = -v[j];
-            st_split32(smem + OFF_WH, smem + OFF_WL, row, 32 * half, v);
-        }
-        proxy_fence();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- U^T += S_0 (-W)^T;  S_0 Q^T ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idw = idesc(64, false, true);
-            const uint32_t idq = idesc(64, false, false);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
+                        }
+                        umma_commit(bar_g);
+                        ++cnt[2];
+                        sp = 1;
+                        progressed = true;
+                    }
+                }
+                if (sp == 1) {
+                    if (mbar_test(bar_wuin, jp & 1) && (jp == 0 || mbar_test(bar_ufree, (jp - 1) & 1))) {
+                        tc_fence_after();
+                        // W^T = K^T T1^T, U~^T = V^T T2^T
+                        const uint32_t inV = sbase + OFF_V;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bwh = sdesc(sbase + OFF_WH + kk * 2048, 16384, 1024);
-                const uint64_t bwl = sdesc(sbase + OFF_WL + kk * 2048, 16384, 1024);
-                const uint32_t ah = tbase + T_SH + 8 * kk, al = tbase + T_SL + 8 * kk;
-                umma_ts(tbase + T_U, ah, bwh, idw, 1);
-                umma_ts(tbase + T_U, ah, bwl, idw, 1);
-                umma_ts(tbase + T_U, al, bwh, idw, 1);
-                if (rd) {
-                    const uint64_t bq = sdesc(inKQ + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    umma_ts(tbase + T_O, ah, bq, idq, kk > 0);
-                    umma_ts(tbase + T_O, al, bq, idq, 1);
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
+                            const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
+                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
+                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
+                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
+                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
+                        }
+                        umma_commit(bar_wu);
+                        ++cnt[3];
+                        progressed = true;
+                        if (ring[jp % kRing].last) prep_done = true;
+                        else {
+                            ++jp;
+                            sp = 0;
+                        }
+                    }
                 }
             }
-            umma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!mma_wait()) { ok = false; break; }
-        mma_pending = false;
-
-        // ---- U'' = c_t U as bf16 hi/lo (K-major A operand [d_v][t]) ----
-        {
-            float v[32];
-            tmem_ld32(trow + T_U + 32 * half, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] *= sc_c[32 * half + j];
-            st_split32(smem + OFF_UH, smem + OFF_UL, row, 32 * half, v);
-        }
-        proxy_fence();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- U''^T P''^T (into the G columns);  St += U''^T K ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idp = idesc(64, false, false);
-            const uint32_t ids = idesc(128, false, true);
-#pragma unroll
-            for (int kt = 0; kt < 4; ++kt) {
-                const uint64_t auh = sdesc(sbase + OFF_UH + kt * 32, 16, 1024);
-                const uint64_t aul = sdesc(sbase + OFF_UL + kt * 32, 16, 1024);
-                if (rd) {
-                    const uint64_t bph = sdesc(sbase + OFF_PH + kt * 32, 16, 1024);
-                    const uint64_t bpl = sdesc(sbase + OFF_PL + kt * 32, 16, 1024);
-                    umma_ss(tbase + T_G, auh, bph, idp, kt > 0);
-                    umma_ss(tbase + T_G, auh, bpl, idp, 1);
-                    umma_ss(tbase + T_G, aul, bph, idp, 1);
+            if (progressed) {
+                t_last = global_ns();
+            } else {
+                __nanosleep(20);
+                if (*abort_flag) break;
+                if (global_ns() - t_last > limit) {
+                    *abort_flag = 1;
+                    break;
                 }
-                const uint64_t bk = sdesc(inKQ + kt * 2048, 16384, 1024);   // K: MN-major over d_k
-                umma_ss(tbase + T_S, auh, bk, ids, 1);
-                umma_ss(tbase + T_S, aul, bk, ids, 1);
-            }
-            umma_commit(bar_mma);
-        }
-        mma_pending = true;
-        if (!mma_wait()) { ok = false; break; }
-        mma_pending = false;
-
-        // ---- readout o_t = gamma_t (S_0 Q^T)[:, t] + (U''^T P''^T)[:, t] ----
-        if (rd) {
-            float a[32], b[32];
-            tmem_ld32(trow + T_O + 32 * half, a);
-            tmem_ld32(trow + T_G + 32 * half, b);
-            OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)h * D + row;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = 32 * half + j;
-                if (t < clen) {
-                    const float ov = fmaf(sc_g[t], a[j], b[j]);
-                    OutT* op = ob + (size_t)(o_row0 + cur.begin + t) * (size_t)H * D;
-                    if constexpr (OUT_BF16)
-                        *op = __float2bfloat16_rn(ov);
-                    else
-                        *op = ov;
-                }
-            }
-        }
-        // ---- running scale; fold it into St at checkpoints, at the end and below the floor ----
-        sigma = single ? 1.f : sigma0 * sc_g[clen - 1];
-        const int chunk_end = cur.begin + clen;
-        while (ck_dump < ck_end && p.ckpts[ck_dump].pos < chunk_end) ++ck_dump;
-        const bool dump = ck_dump < ck_end && p.ckpts[ck_dump].pos == chunk_end;
-        const bool last = chunk_end >= len;
-        if (dump || last || sigma < kSigmaFloor) {
-            float* d1 = dump ? p.ckpt_states + (size_t)p.ckpts[ck_dump].slot * (size_t)H * D * D + head_state : nullptr;
-            float* d2 = (last && job.s_final) ? job.s_final + head_state : nullptr;
-#pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                const int c0 = 64 * half + 32 * cb;
-                float v[32];
-                tmem_ld32(trow + T_S + c0, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= sigma;
-                tmem_st32(trow + T_S + c0, v);
-                if (d1) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(d1 + (size_t)row * D + c0 + j) =
-                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                }
-                if (d2) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(d2 + (size_t)row * D + c0 + j) =
-                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                }
-            }
-            tmem_st_wait();
-            sigma = 1.f;
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        cur = nxt;
-        ++chunk_no;
-    }
-
-    if (ok && len == 0 && job.s_final) {
-        // empty range: the final state is the initial one
-        const float* s0 = job.s0;
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-            const int c0 = 64 * half + 32 * cb;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (s0) x = __ldg(reinterpret_cast<const float4*>(s0 + head_state + (size_t)row * D + c0 + j));
-                *reinterpret_cast<float4*>(job.s_final + head_state + (size_t)row * D + c0 + j) = x;
             }
         }
     }
-    if (!ok && tid == 0) {
-        // never leave with a copy or an MMA still writing into this CTA's shared memory or TMEM
-        for (int cc = chunk_no; cc < kq_issued; ++cc) {
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(&bar_in[cc & 1], (uint32_t)((cc >> 1) & 1)))
-                if (global_ns() - t0 > drain_limit) break;
+
+    // ---- leave only with no copy and no MMA still writing into this CTA's shared memory or TMEM ----
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && *abort_flag) {
+        const int kq = cnt[0];
+        for (int b = 0; b < 2; ++b) {
+            const int c = ((kq - 1) & 1) == b ? kq - 1 : kq - 2;
+            if (c >= 0) drain_phase(&bar_kq[b], (uint32_t)((c >> 1) & 1), drain_limit);
         }
-        for (int cc = chunk_no; cc < v_issued; ++cc) {
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(bar_v, (uint32_t)(cc & 1)))
-                if (global_ns() - t0 > drain_limit) break;
-        }
-        if (mma_pending) {
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(bar_mma, (mma_phase - 1) & 1))
-                if (global_ns() - t0 > drain_limit) break;
-        }
+        if (cnt[1] > 0) drain_phase(bar_v, (uint32_t)((cnt[1] - 1) & 1), drain_limit);
+        for (int i = 0; i < 5; ++i)
+            if (cnt[2 + i] > 0) drain_phase(&bars[3 + i], (uint32_t)((cnt[2 + i] - 1) & 1), drain_limit);
         atomicOr(p.status, STATUS_TIMEOUT);
     }
-    tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(512));
