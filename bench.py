@@ -278,6 +278,32 @@ def time_oracle(jobs, threads: int) -> float:
     return time.perf_counter() - t
 
 
+def placement_report(N: int = 8192, M: int = 16, n_requests: int = 10000):
+    """Checkpoint placement ("Sparse prefix caching ...", sections 3-5) on the seeded depth
+    distributions: expected recompute per request and tokens saved per checkpoint for every
+    strategy at the prefill workload's N and M, and the host time of the O(N M) programme at the
+    long-prefill size (N = 131072, M = 32)."""
+    import hybrid_model_recurrent_gb300 as gdn
+    out = {"N": N, "M": M, "requests": n_requests, "unit": "tokens", "distributions": {}}
+    for kind in synth.DEPTH_KINDS:
+        w = synth.depth_weights(kind, N, n_requests, seed=0)
+        tot = sum(w)
+        none = gdn.gdn_expected_recompute(w, [])
+        row = {"no_cache_per_request": none / tot}
+        for strat in ("balanced", "block", "random", "greedy", "dp"):
+            _, cost = gdn.gdn_ckpt_placement(w, M, strat, seed=0)
+            row[strat] = {"recompute_per_request": cost / tot, "saved_per_checkpoint": (none - cost) / tot / M}
+        out["distributions"][kind] = row
+    wl = synth.depth_weights("prompts", 131072, 20000, seed=0)
+    gdn.gdn_ckpt_placement(wl, 32, "dp")
+    reps = 5
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        gdn.gdn_ckpt_placement(wl, 32, "dp")
+    out["dp_ms_N131072_M32"] = (time.perf_counter() - t0) / reps * 1e3
+    return out
+
+
 def cpu_baseline(w: synth.Workload):
     threads = os.cpu_count() or 1
     pairs = [(b, h) for b in range(w.B) for h in range(w.H)][: 2 * threads]
@@ -433,6 +459,7 @@ def run_ours(args, ws, rank, local):
             "phases": {k: v for k, v in step.tok_head.items()},
             "states_per_s": sum(len(c) for c in step.ck) * w.H * args.steps / slowest,
             "cpu_baseline": base,
+            "placement": placement_report(),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

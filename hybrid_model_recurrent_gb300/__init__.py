@@ -29,6 +29,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn_scan.so")
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = range(5)
 GDN_F32, GDN_BF16 = 0, 1
 ALGO = {"auto": 0, "per_token": 1, "chunked": 2, "chunked_mma": 3}
+PLACE = {"dp": 0, "balanced": 1, "block": 2, "random": 3, "greedy": 4}
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +72,8 @@ def lib():
                                           vp]
             L.gdn_replay_plan.argtypes = [i64, i32, i32, pi64, pi64]
             L.gdn_select_ckpt.argtypes = [pi64, i32, i64, pi32]
+            L.gdn_ckpt_placement.argtypes = [pi64, i64, i32, ctypes.c_int, ctypes.c_uint64, i64, pi64, pi32, pi64]
+            L.gdn_expected_recompute.argtypes = [pi64, i64, pi64, i32, pi64]
             L.gdn_workspace_size.argtypes = []
             L.gdn_workspace_size.restype = sz
             L.gdn_clear_status.argtypes = [vp, sz, vp]
@@ -171,6 +174,31 @@ def gdn_select_ckpt(c: Sequence[int], d: int) -> int:
     _check(lib().gdn_select_ckpt(_p64(arr) if len(arr) else None, len(arr), d, ctypes.byref(j)),
            "gdn_select_ckpt")
     return j.value
+
+
+def gdn_ckpt_placement(weights: Sequence[int], M: int, strategy: str = "dp", seed: int = 0, block: int = 0):
+    """Checkpoint positions for a prefix of N = len(weights) - 1 tokens and depth weights w[0..N].
+
+    Returns (positions, R) with positions strictly increasing in [1, N] and R = sum_d w[d] f(d)
+    the exact expected-recompute numerator of that placement."""
+    w = _i64(weights)
+    N = len(w) - 1
+    out = np.zeros(max(int(M), 1), dtype=np.int64)
+    n = ctypes.c_int32()
+    cost = ctypes.c_int64()
+    _check(lib().gdn_ckpt_placement(_p64(w), N, int(M), PLACE[strategy], ctypes.c_uint64(int(seed)), int(block),
+                                    _p64(out), ctypes.byref(n), ctypes.byref(cost)), "gdn_ckpt_placement")
+    return [int(x) for x in out[:n.value]], cost.value
+
+
+def gdn_expected_recompute(weights: Sequence[int], positions: Sequence[int]) -> int:
+    """R = sum_d w[d] f(d) of a placement (exact integer)."""
+    w = _i64(weights)
+    pos = _i64(positions)
+    cost = ctypes.c_int64()
+    _check(lib().gdn_expected_recompute(_p64(w), len(w) - 1, _p64(pos) if len(pos) else None, len(pos),
+                                        ctypes.byref(cost)), "gdn_expected_recompute")
+    return cost.value
 
 
 def _problem(cu: np.ndarray, H: int, dk: int, dv: int, qkv_dtype: torch.dtype, out_dtype: torch.dtype,

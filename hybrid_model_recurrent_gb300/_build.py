@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", "gdn_scan")
 LIB = os.path.join(PKG, "libgdn_scan.so")
-SOURCES = ["gdn_api.cu", "gdn_noalloc.cu", "inst_chunk_tc.cu", "inst_dk32.cu", "inst_dk64.cu", "inst_dk128.cu"]
+SOURCES = ["gdn_api.cu", "gdn_noalloc.cu", "gdn_placement.cpp", "inst_chunk_tc.cu", "inst_dk32.cu", "inst_dk64.cu", "inst_dk128.cu"]
 HEADERS = [os.path.join(CSRC, f) for f in ("gdn_kernel.cuh", "gdn_chunk.cuh", "gdn_chunk_tc.cuh")] + [
     os.path.join(ROOT, "include", "gdn_scan.h")]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
@@ -30,7 +30,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + HEADERS):
             jobs.append(["nvcc", *NVCC_FLAGS, "-c", s, "-o", o])

@@ -223,6 +223,42 @@ gdn_status gdn_replay_plan(int64_t m, int32_t r_num, int32_t r_den, int64_t* a, 
  * the initial state).  GDN_ERR_INVALID_ARG when c is not strictly increasing. */
 gdn_status gdn_select_ckpt(const int64_t* c, int32_t M, int64_t d, int32_t* j);
 
+/* --- checkpoint placement (host only) -------------------------------------------------
+ * "Sparse prefix caching in hybrid and recurrent LLM serving", sections 3-5.  A
+ * cached prefix of N tokens keeps states at 1 <= c_1 < ... < c_M <= N; a request
+ * overlapping it to depth d recomputes f(d) = d - max{c_i <= d} tokens (the start,
+ * c_0 = 0, when no c_i <= d; f(0) = 0).  The depth distribution is given as integer
+ * weights w[0..N] (host array, w[d] >= 0, e.g. counts of observed depths), so the
+ * expected recompute is the exact integer numerator R = sum_d w[d] f(d) (divide by
+ * sum_d w[d] for tokens per request).  Inputs must satisfy 1 <= N < 2^31 and
+ * sum_d d w[d] < 2^60 and N sum_d w[d] < 2^60 (else GDN_ERR_UNSUPPORTED). */
+typedef enum gdn_placement {
+    GDN_PLACE_DP = 0,        /* optimal: dynamic programme of Theorem 2 in O(N M)
+                                (monotone convex-hull trick); needs (M+1)(N+1) <= 2^26 */
+    GDN_PLACE_BALANCED = 1,  /* Theorem 1: M+1 gaps summing to N+1 that differ by at
+                                most one, the larger ones first (optimal for uniform d) */
+    GDN_PLACE_BLOCK = 2,     /* block boundaries b, 2b, ... <= N, at most M of them;
+                                b = `block`, or floor(N/M) when block = 0 */
+    GDN_PLACE_RANDOM = 3,    /* M distinct positions: the first M draws of a Fisher-Yates
+                                shuffle of 1..N driven by splitmix64(seed), sorted; N <= 2^24 */
+    GDN_PLACE_GREEDY = 4     /* M times the free position that lowers R most (the
+                                shallowest on ties); N <= 2^24 */
+} gdn_placement;
+
+/* Choose checkpoint positions.  M >= 0 is the budget; when M > N every position is
+ * taken.  positions: host int64 [M], written strictly increasing in [1, N]; *count:
+ * how many were written (M, or min(M, N), or fewer for GDN_PLACE_BLOCK); *cost: R of
+ * the written placement.  GDN_ERR_INVALID_ARG on a null pointer, negative weight,
+ * M < 0, block < 0 or an unknown strategy; nothing is written then. */
+gdn_status gdn_ckpt_placement(const int64_t* weights, int64_t N, int32_t M, gdn_placement strategy,
+                              uint64_t seed, int64_t block, int64_t* positions, int32_t* count,
+                              int64_t* cost);
+
+/* R = sum_d w[d] f(d) of a given placement positions[0..M) (host, strictly
+ * increasing in [1, N]); GDN_ERR_INVALID_ARG otherwise. */
+gdn_status gdn_expected_recompute(const int64_t* weights, int64_t N, const int64_t* positions, int32_t M,
+                                  int64_t* cost);
+
 /* Bytes of workspace every device entry point needs. */
 size_t gdn_workspace_size(void);
 

@@ -14,7 +14,9 @@ pages out of one scan primitive:
 * resume from the deepest checkpoint at or below the overlap depth d and
   recompute c_j+1 .. d (same section);
 * Tail-Replay ("Tail-Replay ..." notes page, sections 2.1-2.2): k = ceil(r m),
-  a = m - k, zero state at a, run tokens a+1 .. m; optional exact twin from S_a.
+  a = m - k, zero state at a, run tokens a+1 .. m; optional exact twin from S_a;
+* checkpoint placement (``oracle.placement``; "Sparse prefix caching ...",
+  sections 3-5).
 """
 from __future__ import annotations
 
@@ -56,7 +58,8 @@ def _load():
             lib.gdn_oracle_select_ckpt.argtypes = [vp, i32, i64, ctypes.POINTER(i32)]
             lib.gdn_oracle_scan.argtypes = [ctypes.c_int, ctypes.c_int, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp,
                                             vp, vp]
-            for f in ("gdn_oracle_replay_plan", "gdn_oracle_select_ckpt", "gdn_oracle_scan"):
+            lib.gdn_oracle_place_dp.argtypes = [vp, i64, i32, vp, ctypes.POINTER(i64)]
+            for f in ("gdn_oracle_replay_plan", "gdn_oracle_select_ckpt", "gdn_oracle_scan", "gdn_oracle_place_dp"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib

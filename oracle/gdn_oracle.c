@@ -138,3 +138,70 @@ ORACLE_API int gdn_oracle_scan(int dk, int dv, int64_t n, const double* q, const
     free(u);
     return 0;
 }
+
+/* "Sparse prefix caching in hybrid and recurrent LLM serving", section 3 and section 4, Theorem 2:
+ * the least expected recompute over placements of min(M, N) checkpoints, by the plain dynamic
+ * programme DP[k][t] = min_{k-1 <= s < t} DP[k-1][s] + C(s, t) with DP[0][0] = 0 (the start is the
+ * implicit checkpoint c_0 = 0), C(s, t) = sum_{d=s}^{t-1} w[d] (d - s) read from prefix sums, and
+ * the last segment [c_M, N] closed by C(c_M, N + 1).  O(M N^2) with exact integer costs; ties go to
+ * the smallest s and t.  Returns 0, or 2 when memory runs out. */
+int gdn_oracle_place_dp(const int64_t* w, int64_t N, int32_t M, int64_t* pos, int64_t* cost) {
+    if (M > N) M = (int32_t)N;
+    const size_t n1 = (size_t)N + 2;
+    int64_t* W0 = (int64_t*)calloc(n1, sizeof(int64_t));
+    int64_t* W1 = (int64_t*)calloc(n1, sizeof(int64_t));
+    int64_t* E = (int64_t*)malloc((size_t)(M + 1) * (size_t)(N + 1) * sizeof(int64_t));
+    int64_t* par = (int64_t*)malloc((size_t)(M + 1) * (size_t)(N + 1) * sizeof(int64_t));
+    if (!W0 || !W1 || !E || !par) {
+        free(W0);
+        free(W1);
+        free(E);
+        free(par);
+        return 2;
+    }
+    for (int64_t d = 0; d <= N; ++d) {
+        W0[d + 1] = W0[d] + w[d];
+        W1[d + 1] = W1[d] + d * w[d];
+    }
+#define SEG(s, t) ((W1[t] - W1[s]) - (s) * (W0[t] - W0[s]))
+#define AT(a, k, t) a[(size_t)(k) * (size_t)(N + 1) + (size_t)(t)]
+    const int64_t INF = INT64_MAX;
+    for (int64_t t = 0; t <= N; ++t) AT(E, 0, t) = t == 0 ? 0 : INF;
+    for (int32_t k = 1; k <= M; ++k) {
+        for (int64_t t = 0; t <= N; ++t) {
+            AT(E, k, t) = INF;
+            AT(par, k, t) = -1;
+            if (t < k) continue;
+            for (int64_t s = k - 1; s < t; ++s) {
+                if (AT(E, k - 1, s) == INF) continue;
+                const int64_t v = AT(E, k - 1, s) + SEG(s, t);
+                if (v < AT(E, k, t)) {
+                    AT(E, k, t) = v;
+                    AT(par, k, t) = s;
+                }
+            }
+        }
+    }
+    int64_t best = INF, best_t = 0;
+    for (int64_t t = M; t <= N; ++t) {
+        if (AT(E, M, t) == INF) continue;
+        const int64_t v = AT(E, M, t) + SEG(t, N + 1);
+        if (v < best) {
+            best = v;
+            best_t = t;
+        }
+    }
+    int64_t t = best_t;
+    for (int32_t k = M; k >= 1; --k) {
+        pos[k - 1] = t;
+        t = AT(par, k, t);
+    }
+    *cost = best;
+#undef SEG
+#undef AT
+    free(W0);
+    free(W1);
+    free(E);
+    free(par);
+    return 0;
+}

@@ -260,3 +260,41 @@ def make_inputs(w: Workload, device="cpu", t_range: Optional[tuple] = None,
 def state(seed: int, n: int, dv: int, dk: int, scale: float = 1.0, device="cpu", salt: int = 0) -> torch.Tensor:
     """Seeded fp32 states [n, dv, dk] (an arbitrary initial / cached state)."""
     return normal(seed, STREAM_STATE, salt * (1 << 40), (n, dv, dk), scale, device)
+
+
+# --------------------------------------------------------------------------------------------
+# overlap-depth distributions for checkpoint placement
+# --------------------------------------------------------------------------------------------
+DEPTH_KINDS = ("uniform", "prompts", "documents")
+
+
+def depth_weights(kind: str, N: int, n_requests: int, seed: int = 0) -> List[int]:
+    """Integer weights w[0..N]: counts of `n_requests` seeded overlap depths d in [0, N].
+
+    Stand-ins for the pages' measured overlap distributions (document QA and shared system
+    prompts, whose data is not available here):
+      uniform   - d ~ U{1..N};
+      prompts   - three requests in four reuse one of 8 shared prompt lengths (lengths ~ U{1..N},
+                  request's prompt ~ U{0..7}); the rest d ~ U{0..N} (0: no overlap at all);
+      documents - d = floor((u1 + u2) / 2) with u1, u2 ~ U{1..N} (overlaps cluster mid-document),
+                  and one request in ten has no overlap (d = 0)."""
+    if kind not in DEPTH_KINDS:
+        raise ValueError(kind)
+    w = [0] * (N + 1)
+    if kind == "uniform":
+        for d in integers(seed, 101, 0, n_requests, 1, N):
+            w[d] += 1
+    elif kind == "prompts":
+        spikes = integers(seed, 102, 0, 8, 1, N)
+        pick = integers(seed, 103, 0, n_requests, 0, 7)
+        coin = integers(seed, 104, 0, n_requests, 0, 3)
+        other = integers(seed, 105, 0, n_requests, 0, N)
+        for i in range(n_requests):
+            w[spikes[pick[i]] if coin[i] < 3 else other[i]] += 1
+    else:
+        u1 = integers(seed, 106, 0, n_requests, 1, N)
+        u2 = integers(seed, 107, 0, n_requests, 1, N)
+        coin = integers(seed, 108, 0, n_requests, 0, 9)
+        for i in range(n_requests):
+            w[0 if coin[i] == 0 else (u1[i] + u2[i]) // 2] += 1
+    return w

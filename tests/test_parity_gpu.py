@@ -268,6 +268,50 @@ def test_small_alpha_gates(algo):
                 check_output(rs["o"][lo:hi, h], o_["o"], f"small-alpha resume o probe {i} h={h}")
 
 
+@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+def test_placement_feeds_prefill_and_resume(algo):
+    """Checkpoints chosen by the placement programme ("Sparse prefix caching ...", Theorem 2) for a
+    seeded depth distribution drive gdn_prefill_ckpt; resume probes at depths drawn from the same
+    distribution recompute exactly f(d) tokens and match the oracle."""
+    from oracle import placement as PL
+    lens = [400, 257]
+    H = 2
+    w, inp = _inputs(71, lens, H, 128, 128, torch.bfloat16, 0.9, 1.0, beta="sigmoid")
+    cu = w.cu_seqlens
+    ck = []
+    for b, n in enumerate(lens):
+        wd = synth.depth_weights("prompts", n, 3000, seed=b)
+        pos, cost = gdn.gdn_ckpt_placement(wd, 5, "dp")
+        assert cost == PL.place_dp(wd, 5)[1]
+        ck.append(pos)
+    d = _dev(inp)
+    r = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=ck, out_dtype=torch.float32, algo=algo)
+    torch.cuda.synchronize()
+    probes = []
+    for b, n in enumerate(lens):
+        wd = synth.depth_weights("prompts", n, 3000, seed=b)
+        support = [x for x in range(n + 1) if wd[x] > 0]
+        picks = synth.integers(500 + b, 0, 0, 6, 0, len(support) - 1)
+        probes += [(b, support[i]) for i in picks]
+    rs = gdn.gdn_resume_from_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, r["ckpt_states"], ck, probes,
+                                  out_dtype=torch.float32, algo=algo)
+    torch.cuda.synchronize()
+    base = [0, len(ck[0])]
+    for i, (s, dd) in enumerate(probes):
+        assert rs["offsets"][i + 1] - rs["offsets"][i] == PL.recompute(ck[s], dd)
+        sl = slice(cu[s], cu[s + 1])
+        # the oracle resumes from its own checkpoint states (no oracle input comes from the GPU)
+        for h in range(H):
+            refh = _oracle_prefill_head(inp, cu, s, h, ckpt=ck[s])
+            o_ = oracle.resume(inp.q[sl, h], inp.k[sl, h], inp.v[sl, h], inp.alpha[sl, h], inp.beta[sl, h],
+                               [refh["ckpt"][j] for j in range(len(ck[s]))], ck[s], dd)
+            assert rs["chosen"][i] == o_["c"]
+            assert_close(rs["S_out"][i, h], o_["S"], f"placement resume probe {i} h={h}")
+            lo, hi = rs["offsets"][i], rs["offsets"][i + 1]
+            if hi > lo:
+                check_output(rs["o"][lo:hi, h], o_["o"], f"placement resume o probe {i} h={h}")
+
+
 # ---------------------------------------------------------------------------------------------
 # invariants on the GPU
 # ---------------------------------------------------------------------------------------------
