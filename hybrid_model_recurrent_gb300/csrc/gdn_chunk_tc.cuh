@@ -48,6 +48,8 @@
 //   [384,448) St hi (bf16 pairs)   [448,512) St lo
 #pragma once
 
+#include <climits>
+
 #include "gdn_kernel.cuh"
 
 namespace gdn {
@@ -192,6 +194,32 @@ __device__ __forceinline__ void st_split32(unsigned char* th, unsigned char* tl,
         *reinterpret_cast<uint4*>(th + sw128(row, c0 + 8 * q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *reinterpret_cast<uint4*>(tl + sw128(row, c0 + 8 * q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
+}
+// x = hi + lo, both tf32 (10 explicit mantissa bits each)
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
+}
+// d (16 x 8, m16n8 accumulator layout) += A (16 x 8, row-major at a, row stride lda) B (8 x 8, row-major
+// at b, row stride ldb), as hi*hi + hi*lo + lo*hi with mma.sync m16n8k8 tf32 (fp32 accumulate)
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const float* a, int lda, const float* b, int ldb, int g8,
+                                           int t4) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    tf32_split(a[g8 * lda + t4], ah[0], al[0]);
+    tf32_split(a[(g8 + 8) * lda + t4], ah[1], al[1]);
+    tf32_split(a[g8 * lda + t4 + 4], ah[2], al[2]);
+    tf32_split(a[(g8 + 8) * lda + t4 + 4], ah[3], al[3]);
+    tf32_split(b[t4 * ldb + g8], bh[0], bl[0]);
+    tf32_split(b[(t4 + 4) * ldb + g8], bh[1], bl[1]);
+#define GDN_MMA_TF32(A, B)                                                                                      \
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, " \
+                 "{%0,%1,%2,%3};"                                                                               \
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])                                              \
+                 : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(B[0]), "r"(B[1]))
+    GDN_MMA_TF32(al, bh);
+    GDN_MMA_TF32(ah, bl);
+    GDN_MMA_TF32(ah, bh);
+#undef GDN_MMA_TF32
 }
 __device__ __forceinline__ void group_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -529,14 +557,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         const int half = pw >> 2;                // column half of G / W handled by this warp
         const bool leader = ptid == 0;
         // gate warp (pw == 3) state: schedule cursors, running scale, the next window's gates
-        int g_ck_sched = job.ck_begin, g_ck_dump = job.ck_begin;
+        // the next checkpoint not yet reached, cached in registers (the table lives in the parameter block,
+        // where an indexed read is slow): every checkpoint ends a window, so one cursor serves the
+        // schedule and the dumps
+        int g_ck = job.ck_begin;
+        int g_ck_pos = g_ck < ck_end ? p.ckpts[g_ck].pos : INT_MAX;
+        int g_ck_slot = g_ck < ck_end ? p.ckpts[g_ck].slot : -1;
         float g_sigma = 1.f;
         Pos g_win{0, 0};
         float ga0 = 1.f, ga1 = 1.f, gb0 = 0.f, gb1 = 0.f;
-        auto next_window = [&](int pos, int& ck) -> Pos {
+        auto next_window = [&](int pos) -> Pos {   // 64 tokens from pos, cut at the next checkpoint
             int end = pos + C < len ? pos + C : len;
-            while (ck < ck_end && p.ckpts[ck].pos <= pos) ++ck;
-            if (ck < ck_end && p.ckpts[ck].pos < end) end = p.ckpts[ck].pos;
+            if (g_ck_pos < end) end = g_ck_pos;
             return Pos{pos, end - pos};
         };
         auto load_gates = [&](Pos c) {
@@ -591,13 +623,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             const float glast = __shfl_sync(0xffffffffu, n > 32 ? g1 : g0, (n - 1) & 31);
             const bool single = n == 1 && gfirst < kGammaFloor;
             const int chunk_end = g_win.begin + n;
-            while (g_ck_dump < ck_end && p.ckpts[g_ck_dump].pos < chunk_end) ++g_ck_dump;
-            const bool dump = g_ck_dump < ck_end && p.ckpts[g_ck_dump].pos == chunk_end;
+            const bool dump = g_ck_pos == chunk_end;
+            const int dump_slot = g_ck_slot;
+            if (dump) {
+                ++g_ck;
+                g_ck_pos = g_ck < ck_end ? p.ckpts[g_ck].pos : INT_MAX;
+                g_ck_slot = g_ck < ck_end ? p.ckpts[g_ck].slot : -1;
+            }
             const bool last = chunk_end >= len;
             const float sigma0 = g_sigma;
             const float s_after = single ? 1.f : sigma0 * glast;
             const bool fold = dump || last || s_after < kSigmaFloor;
-            const Pos nx = last ? Pos{len, 0} : next_window(chunk_end, g_ck_sched);
+            const Pos nx = last ? Pos{len, 0} : next_window(chunk_end);
             float* ps = psc + (jj & 1) * 4 * C;
             ps[lane] = g0;
             ps[lane + 32] = g1;
@@ -617,7 +654,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 R.n = n;
                 R.single = single ? 1 : 0;
                 R.fold = fold ? 1 : 0;
-                R.dump_slot = dump ? p.ckpts[g_ck_dump].slot : -1;
+                R.dump_slot = dump ? dump_slot : -1;
                 R.last = last ? 1 : 0;
                 R.next_begin = nx.begin;
                 R.next_len = nx.len;
@@ -633,7 +670,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         };
 
         if (pw == 3) {
-            g_win = next_window(0, g_ck_sched);
+            g_win = next_window(0);
             load_gates(g_win);
             if (lane == 0 && allowed(0)) {
                 issue_kq(0, 0);
@@ -642,6 +679,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             compute_chunk(0);
             if (lane == 0 && ring[0].next_len > 0 && allowed(1)) issue_kq(1, ring[0].next_begin);
         }
+        // T is lower triangular: the rows 0-31, columns 32-63 of the T diag(.) operand tiles stay zero
+        for (int i = ptid; i < 4 * 32 * 4; i += NPREP) {
+            const int tile = i >> 7, r = (i >> 2) & 31, q = i & 3;
+            *reinterpret_cast<uint4*>(smem + OFF_T1H + tile * 8192 + sw128(r, 32 + 8 * q)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        proxy_fence();
         group_sync(BAR_PREP, NPREP);
 
         for (int j = 0;; ++j) {
@@ -669,11 +712,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             group_sync(BAR_PREP, NPREP);
             if (leader) mbar_arrive(bar_gin);
 
-            // ---- G = [K; Q] K^T; then L (fp32, zero on and above the diagonal) ----
+            // ---- G = [K; Q] K^T ----
             if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             tc_fence_after();
-            if (lq < 2) {
-                const int t = row, s0 = 32 * half;
+            const int g8 = lane >> 2, t4 = lane & 3;
+            const float* sg_bg = ps + 2 * C;
+            const float* sg_b = ps + 3 * C;
+            // T1 = T diag(beta gamma), T2 = T diag(beta) as bf16 hi/lo, K-major [t][s]: two adjacent columns
+            auto put_t12 = [&](int t, int s, float x0, float x1) {
+                uint32_t h1, l1, h2, l2;
+                split_pair(x0 * sg_bg[s], x1 * sg_bg[s + 1], h1, l1);
+                split_pair(x0 * sg_b[s], x1 * sg_b[s + 1], h2, l2);
+                const uint32_t o = sw128(t, s);
+                *reinterpret_cast<uint32_t*>(smem + OFF_T1H + o) = h1;
+                *reinterpret_cast<uint32_t*>(smem + OFF_T1L + o) = l1;
+                *reinterpret_cast<uint32_t*>(smem + OFF_T2H + o) = h2;
+                *reinterpret_cast<uint32_t*>(smem + OFF_T2L + o) = l2;
+            };
+            // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 4 (rows 0-31 of G, columns
+            //      0-31) and warp 9 (rows 32-63, columns 32-63) each hold a whole diagonal 32-block of L and
+            //      invert it alone: two 16x16 forward substitutions and one merge, then its T operands.
+            //      Warp 5 stages L_BA (rows 32-63, columns 0-31); the gate warp runs a chunk ahead. ----
+            if (pw == 0 || pw == 5 || pw == 1) {
+                const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant of warps 4 / 9
+                const int t = row, s0 = 32 * half;         // warp 4: t 0-31, s 0-31; 9: 32-63, 32-63; 5: 32-63, 0-31
                 float gi[32];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
@@ -683,7 +745,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     gi[i + 2] = x.z;
                     gi[i + 3] = x.w;
                 }
-                const float f = ps[2 * C + t];
+                const float f = sg_bg[t];
                 float v[32];
                 tmem_ld32(trow + T_G + 32 * half, v);
 #pragma unroll
@@ -692,118 +754,114 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 for (int q4 = 0; q4 < 8; ++q4)
                     *reinterpret_cast<float4*>(Lf + t * kLdF + s0 + 4 * q4) =
                         make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-                // the 16x16 diagonal block of row t, if it lies in this half
-                if ((t >> 5) == half) {
-                    const int b0 = (t & 16);   // 0 or 16 within the half
+                if (pw != 1) {
+                    // the 16x16 diagonal block of row t (columns (lane & 16) .. +15 of this half)
                     float* dst = Ld + (t >> 4) * 16 * 17 + (t & 15) * 17;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[i] = (b0 == 0) ? v[i] : v[16 + i];
+                    for (int i = 0; i < 16; ++i) dst[i] = (lane & 16) ? v[16 + i] : v[i];
+                    __syncwarp();
+                    // lanes 0-15: column jc of block 2 qw; lanes 16-31: of block 2 qw + 1 (forward substitution,
+                    // each dot product in four partial sums)
+                    {
+                        const int bb = 2 * qw + (lane >> 4), jc = lane & 15;
+                        const float* Lb = Ld + bb * 16 * 17;
+                        float x[16];
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) {
+                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int s2 = 0; s2 < r; ++s2) acc[s2 & 3] = fmaf(Lb[r * 17 + s2], x[s2], acc[s2 & 3]);
+                            x[r] = ((r == jc) ? 1.f : 0.f) - ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+                        }
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) Lf[(16 * bb + r) * kLdF + 16 * bb + jc] = x[r];
+                    }
+                    __syncwarp();
+                    // merge: T_ib,jb = -T_ib,ib (L_ib,jb T_jb,jb), (jb, ib) = (2 qw, 2 qw + 1), on mma.sync tf32
+                    {
+                        const int jb = 2 * qw, ib = jb + 1;
+                        float* sc = Ld + jb * 16 * 17;   // this warp's diagonal blocks are no longer needed
+                        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int ks = 0; ks < 2; ++ks)
+                                mma_tf32x3(y[nt], Lf + (16 * ib) * kLdF + 16 * jb + 8 * ks, kLdF,
+                                           Lf + (16 * jb + 8 * ks) * kLdF + 16 * jb + 8 * nt, kLdF, g8, t4);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            sc[g8 * 16 + 8 * nt + 2 * t4] = y[nt][0];
+                            sc[g8 * 16 + 8 * nt + 2 * t4 + 1] = y[nt][1];
+                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4] = y[nt][2];
+                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4 + 1] = y[nt][3];
+                        }
+                        __syncwarp();
+                        float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int ks = 0; ks < 2; ++ks)
+                                mma_tf32x3(x[nt], Lf + (16 * ib) * kLdF + 16 * ib + 8 * ks, kLdF, sc + 8 * ks * 16 + 8 * nt,
+                                           16, g8, t4);
+                        float* dst = Lf + (16 * ib) * kLdF + 16 * jb;
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            dst[g8 * kLdF + 8 * nt + 2 * t4] = -x[nt][0];
+                            dst[g8 * kLdF + 8 * nt + 2 * t4 + 1] = -x[nt][1];
+                            dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4] = -x[nt][2];
+                            dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4 + 1] = -x[nt][3];
+                        }
+                    }
+                    __syncwarp();
+                    // this 32-block's T operands: row t, columns s0 .. s0 + 31, 8 columns per 16-byte store
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 x0 = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + 8 * q);
+                        const float4 x1 = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + 8 * q + 4);
+                        const float4 a0 = *reinterpret_cast<const float4*>(sg_bg + s0 + 8 * q);
+                        const float4 a1 = *reinterpret_cast<const float4*>(sg_bg + s0 + 8 * q + 4);
+                        const float4 b0 = *reinterpret_cast<const float4*>(sg_b + s0 + 8 * q);
+                        const float4 b1 = *reinterpret_cast<const float4*>(sg_b + s0 + 8 * q + 4);
+                        uint32_t h1[4], l1[4], h2[4], l2[4];
+                        split_pair(x0.x * a0.x, x0.y * a0.y, h1[0], l1[0]);
+                        split_pair(x0.z * a0.z, x0.w * a0.w, h1[1], l1[1]);
+                        split_pair(x1.x * a1.x, x1.y * a1.y, h1[2], l1[2]);
+                        split_pair(x1.z * a1.z, x1.w * a1.w, h1[3], l1[3]);
+                        split_pair(x0.x * b0.x, x0.y * b0.y, h2[0], l2[0]);
+                        split_pair(x0.z * b0.z, x0.w * b0.w, h2[1], l2[1]);
+                        split_pair(x1.x * b1.x, x1.y * b1.y, h2[2], l2[2]);
+                        split_pair(x1.z * b1.z, x1.w * b1.w, h2[3], l2[3]);
+                        const uint32_t o = sw128(t, s0 + 8 * q);
+                        *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+                        *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+                        *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                        *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+                    }
                 }
             } else if (pw == 3 && !last) {
                 compute_chunk(j + 1);   // the gate warp runs one chunk ahead
             }
             group_sync(BAR_PREP, NPREP);
-
-            // ---- T = (I + L)^-1 in place over Lf: 16x16 diagonal inverses, then a two-level merge ----
-            if (pw < 4 && lane < 16) {
-                const int b = pw, jc = lane;
-                const float* Lb = Ld + b * 16 * 17;
-                float x[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float vv = (t == jc) ? 1.f : 0.f;
-#pragma unroll
-                    for (int s2 = 0; s2 < t; ++s2) vv = fmaf(-Lb[t * 17 + s2], x[s2], vv);
-                    x[t] = vv;
-                }
-#pragma unroll
-                for (int t = 0; t < 16; ++t) Lf[(16 * b + t) * kLdF + 16 * b + jc] = x[t];
-            }
-            group_sync(BAR_PREP, NPREP);
-            {   // T_10 = -T_11 L_10 T_00 (threads 0-127) and T_32 = -T_33 L_32 T_22 (threads 128-255)
-                const int grp = ptid >> 7, tg = ptid & 127;
-                const int jb = 2 * grp, ib = jb + 1;
-                const int r = tg >> 3, c = 2 * (tg & 7);
-                float* Y = Yb + grp * 16 * 17;
-                float y0 = 0.f, y1 = 0.f;
-                const float* Lr = Lf + (16 * ib + r) * kLdF + 16 * jb;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float l = Lr[m];
-                    const float2 tv = *reinterpret_cast<const float2*>(Lf + (16 * jb + m) * kLdF + 16 * jb + c);
-                    y0 = fmaf(l, tv.x, y0);
-                    y1 = fmaf(l, tv.y, y1);
-                }
-                Y[r * 17 + c] = y0;
-                Y[r * 17 + c + 1] = y1;
-                group_sync(BAR_PREP_A + grp, 128);
-                float x0 = 0.f, x1 = 0.f;
-                const float* Ti = Lf + (16 * ib + r) * kLdF + 16 * ib;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float tv = Ti[m];
-                    x0 = fmaf(tv, Y[m * 17 + c], x0);
-                    x1 = fmaf(tv, Y[m * 17 + c + 1], x1);
-                }
-                Lf[(16 * ib + r) * kLdF + 16 * jb + c] = -x0;
-                Lf[(16 * ib + r) * kLdF + 16 * jb + c + 1] = -x1;
-            }
-            group_sync(BAR_PREP, NPREP);
-            {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block
-                const int r = ptid >> 3, c = 4 * (ptid & 7);
+            {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block on mma.sync tf32; warp = (row, column) tile
+                const int mt = pw >> 2, nt = pw & 3;
                 float y[4] = {0.f, 0.f, 0.f, 0.f};
-                const float* Lr = Lf + (32 + r) * kLdF;
-#pragma unroll 8
-                for (int m = 0; m < 32; ++m) {
-                    const float l = Lr[m];
-                    const float4 tv = *reinterpret_cast<const float4*>(Lf + m * kLdF + c);
-                    y[0] = fmaf(l, tv.x, y[0]);
-                    y[1] = fmaf(l, tv.y, y[1]);
-                    y[2] = fmaf(l, tv.z, y[2]);
-                    y[3] = fmaf(l, tv.w, y[3]);
-                }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) Yb[r * 33 + c + e] = y[e];
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32x3(y, Lf + (32 + 16 * mt) * kLdF + 8 * ks, kLdF, Lf + (8 * ks) * kLdF + 8 * nt, kLdF,
+                               g8, t4);
+                // L_BA T_AA as [32][33] scratch
+                Yb[(16 * mt + g8) * 33 + 8 * nt + 2 * t4] = y[0];
+                Yb[(16 * mt + g8) * 33 + 8 * nt + 2 * t4 + 1] = y[1];
+                Yb[(16 * mt + g8 + 8) * 33 + 8 * nt + 2 * t4] = y[2];
+                Yb[(16 * mt + g8 + 8) * 33 + 8 * nt + 2 * t4 + 1] = y[3];
                 group_sync(BAR_PREP, NPREP);
                 float x[4] = {0.f, 0.f, 0.f, 0.f};
-                const float* Tr = Lf + (32 + r) * kLdF + 32;
-#pragma unroll 8
-                for (int m = 0; m < 32; ++m) {
-                    const float tv = Tr[m];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) x[e] = fmaf(tv, Yb[m * 33 + c + e], x[e]);
-                }
-                *reinterpret_cast<float4*>(Lf + (32 + r) * kLdF + c) = make_float4(-x[0], -x[1], -x[2], -x[3]);
-            }
-            group_sync(BAR_PREP, NPREP);
-            // ---- T1 = T diag(beta gamma), T2 = T diag(beta) as bf16 hi/lo, K-major [t][s] ----
-            {
-                const int t = ptid >> 2, s0 = 16 * (ptid & 3);
-                float tv[16], bg[16], bb[16];
-#pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + i);
-                    const float4 y = *reinterpret_cast<const float4*>(ps + 2 * C + s0 + i);
-                    const float4 z = *reinterpret_cast<const float4*>(ps + 3 * C + s0 + i);
-                    tv[i] = x.x; tv[i + 1] = x.y; tv[i + 2] = x.z; tv[i + 3] = x.w;
-                    bg[i] = y.x; bg[i + 1] = y.y; bg[i + 2] = y.z; bg[i + 3] = y.w;
-                    bb[i] = z.x; bb[i + 1] = z.y; bb[i + 2] = z.z; bb[i + 3] = z.w;
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t ah[4], al[4], bh[4], bl[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 8 * q + 2 * e;
-                        split_pair(tv[i] * bg[i], tv[i + 1] * bg[i + 1], ah[e], al[e]);
-                        split_pair(tv[i] * bb[i], tv[i + 1] * bb[i + 1], bh[e], bl[e]);
-                    }
-                    const uint32_t o = sw128(t, s0 + 8 * q);
-                    *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-                    *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(al[0], al[1], al[2], al[3]);
-                    *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-                    *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32x3(x, Lf + (32 + 16 * mt) * kLdF + 32 + 8 * ks, kLdF, Yb + (8 * ks) * 33 + 8 * nt, 33,
+                               g8, t4);
+                put_t12(32 + 16 * mt + g8, 8 * nt + 2 * t4, -x[0], -x[1]);
+                put_t12(32 + 16 * mt + g8 + 8, 8 * nt + 2 * t4, -x[2], -x[3]);
             }
             proxy_fence();
             group_sync(BAR_PREP, NPREP);
@@ -855,6 +913,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         const uint32_t id128b = idesc(128, false, true);
         while (!(chain_done && prep_done)) {
             bool progressed = false;
+            if (!prep_done) {
+                const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
+                if (sp == 0) {
+                    if (mbar_test(bar_gin, jp & 1)) {
+                        tc_fence_after();
+                        // G = [K; Q] K^T
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
+                        }
+                        umma_commit(bar_g);
+                        ++cnt[2];
+                        sp = 1;
+                        progressed = true;
+                    }
+                }
+                if (sp == 1) {
+                    if (mbar_test(bar_wuin, jp & 1) && (jp == 0 || mbar_test(bar_ufree, (jp - 1) & 1))) {
+                        tc_fence_after();
+                        // W^T = K^T T1^T, U~^T = V^T T2^T
+                        const uint32_t inV = sbase + OFF_V;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
+                            const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
+                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
+                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
+                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
+                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
+                        }
+                        umma_commit(bar_wu);
+                        ++cnt[3];
+                        progressed = true;
+                        if (ring[jp % kRing].last) prep_done = true;
+                        else {
+                            ++jp;
+                            sp = 0;
+                        }
+                    }
+                }
+            }
             if (!chain_done) {
                 const Ring& R = ring[jc % kRing];
                 const uint32_t inKQ = sbase + OFF_KQ + (jc & 1) * 32768;
@@ -936,48 +1036,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     else {
                         ++jc;
                         sc = 0;
-                    }
-                }
-            }
-            if (!prep_done) {
-                const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
-                if (sp == 0) {
-                    if (mbar_test(bar_gin, jp & 1)) {
-                        tc_fence_after();
-                        // G = [K; Q] K^T
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
-                        }
-                        umma_commit(bar_g);
-                        ++cnt[2];
-                        sp = 1;
-                        progressed = true;
-                    }
-                }
-                if (sp == 1) {
-                    if (mbar_test(bar_wuin, jp & 1) && (jp == 0 || mbar_test(bar_ufree, (jp - 1) & 1))) {
-                        tc_fence_after();
-                        // W^T = K^T T1^T, U~^T = V^T T2^T
-                        const uint32_t inV = sbase + OFF_V;
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
-                            const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
-                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
-                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
-                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
-                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
-                        }
-                        umma_commit(bar_wu);
-                        ++cnt[3];
-                        progressed = true;
-                        if (ring[jp % kRing].last) prep_done = true;
-                        else {
-                            ++jp;
-                            sp = 0;
-                        }
                     }
                 }
             }
