@@ -34,17 +34,19 @@
 // Three warp roles run a software pipeline over the chunks of one (job, head):
 //   chain (warps 0-3) - the state-dependent conversions of chunk j: St into the bf16 A operand,
 //       U'' from U, readout, checkpoints;
-//   prep (warps 4-11) - the state-independent conversions of chunk j+1: L from G, T, the
+//   prep (warps 4-11) - the state-independent work of chunk j+1: G, L, T, the
 //       T diag(.) operands, -sigma_0 W, P, and (one warp) the gates and the chunk schedule one
 //       chunk further ahead;
 //   issue (warp 12, one lane) - every tcgen05.mma: the chain's U^T += St (-sigma_0 W)^T, St Q^T,
-//       St += U''^T K, U''^T P^T and the prep's G = [K; Q] K^T, W^T, U~^T, each as soon as the
+//       St += U''^T K, U''^T P^T and the prep's [K; Q] K^T (for P), W^T, U~^T, each as soon as the
 //       mbarriers of its operands have fired, so that no converting warp waits on a full MMA queue.
+// K K^T for L, on the prep stage's critical path, runs on mma.sync inside the prep warps (exact bf16
+// inputs), which turn its accumulators into L directly.
 // They hand over through mbarriers; each group agrees on every wait by a barrier reduction, so a
 // wait that runs out ends every loop without leaving a named barrier half-entered.
 //
 // TMEM (512 columns x 128 lanes of 32 bit):
-//   [0,128) St   [128,192) U^T   [192,256) O^T   [256,320) G   [320,384) W^T
+//   [0,128) St   [128,192) U^T   [192,256) O^T   [256,320) [K; Q] K^T   [320,384) W^T
 //   [384,448) St hi (bf16 pairs)   [448,512) St lo
 #pragma once
 
@@ -195,6 +197,23 @@ __device__ __forceinline__ void st_split32(unsigned char* th, unsigned char* tl,
         *reinterpret_cast<uint4*>(tl + sw128(row, c0 + 8 * q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
 }
+// mma.sync m16n8k16 (row.col, bf16 -> f32) with operands from ldmatrix
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// byte offset of element (row, col) in the [K; Q] buffer (two 64-column blocks of [128 rows][128 B]); col % 8 == 0
+__device__ __forceinline__ uint32_t kq_off(int row, int col) {
+    return (uint32_t)((col >> 6) * 16384) + sw128(row, col & 63);
+}
 // x = hi + lo, both tf32 (10 explicit mantissa bits each)
 __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     // TMA and MMA completions (one arrival each)
     uint64_t* bar_kq = bars + 0;       // [2] K/Q tiles landed
     uint64_t* bar_v = bars + 2;        // V tile landed
-    uint64_t* bar_g = bars + 3;        // G done
+    uint64_t* bar_g = bars + 3;        // [K; Q] K^T done (its Q rows give P)
     uint64_t* bar_wu = bars + 4;       // W^T, U~^T done
     uint64_t* bar_uo = bars + 5;       // U^T done
     uint64_t* bar_st = bars + 6;       // state update and every MMA issued before it done
@@ -710,12 +729,55 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             }
             tc_fence_before();
             group_sync(BAR_PREP, NPREP);
-            if (leader) mbar_arrive(bar_gin);
+            if (leader) mbar_arrive(bar_gin);   // [K; Q] K^T on tcgen05, for P at the end of this iteration
 
-            // ---- G = [K; Q] K^T ----
-            if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
-            tc_fence_after();
+            // ---- K K^T on mma.sync (exact bf16 inputs) for L: warp = (row tile mt, column half); column tiles
+            //      wholly above the diagonal are zero in L and skipped ----
             const int g8 = lane >> 2, t4 = lane & 3;
+            {
+                const uint32_t inKQ = sbase + OFF_KQ + (j & 1) * 32768;
+                const int mt = pw >> 1, nb = 32 * (pw & 1);
+                const int njp = (nb >= 16 * (mt + 1)) ? 0 : (nb + 16 >= 16 * (mt + 1) ? 1 : 2);   // live column pairs
+                float ga[4][4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) ga[jj][e] = 0.f;
+                if (njp > 0) {
+#pragma unroll
+                    for (int kt = 0; kt < 8; ++kt) {
+                        uint32_t ak[4];
+                        ldsm4(inKQ + kq_off(16 * mt + (lane & 15), 16 * kt + 8 * (lane >> 4)), ak);
+#pragma unroll
+                        for (int jp = 0; jp < 2; ++jp) {
+                            if (jp < njp) {
+                                uint32_t b[4];
+                                ldsm4(inKQ + kq_off(nb + 16 * jp + 8 * (lane >> 4) + (lane & 7), 16 * kt + 8 * ((lane >> 3) & 1)),
+                                      b);
+                                mma_bf16(ga[2 * jp], ak, b[0], b[1]);
+                                mma_bf16(ga[2 * jp + 1], ak, b[2], b[3]);
+                            }
+                        }
+                    }
+                }
+                // L[t][s] = beta_t gamma_t / gamma_s (k_t . k_s) for s < t, else 0; diagonal 16-blocks also to Ld
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int t = 16 * mt + g8 + 8 * hh, s2 = nb + 8 * jj + 2 * t4;
+                        const float f = ps[2 * C + t];
+                        const float l0 = s2 < t ? f * ps[C + s2] * ga[jj][2 * hh] : 0.f;
+                        const float l1 = s2 + 1 < t ? f * ps[C + s2 + 1] * ga[jj][2 * hh + 1] : 0.f;
+                        *reinterpret_cast<float2*>(Lf + t * kLdF + s2) = make_float2(l0, l1);
+                        if ((s2 >> 4) == (t >> 4)) {
+                            float* dd = Ld + (t >> 4) * 16 * 17 + (t & 15) * 17 + (s2 & 15);
+                            dd[0] = l0;
+                            dd[1] = l1;
+                        }
+                    }
+            }
+            group_sync(BAR_PREP, NPREP);
             const float* sg_bg = ps + 2 * C;
             const float* sg_b = ps + 3 * C;
             // T1 = T diag(beta gamma), T2 = T diag(beta) as bf16 hi/lo, K-major [t][s]: two adjacent columns
@@ -730,36 +792,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 *reinterpret_cast<uint32_t*>(smem + OFF_T2L + o) = l2;
             };
             // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 4 (rows 0-31 of G, columns
-            //      0-31) and warp 9 (rows 32-63, columns 32-63) each hold a whole diagonal 32-block of L and
-            //      invert it alone: two 16x16 forward substitutions and one merge, then its T operands.
-            //      Warp 5 stages L_BA (rows 32-63, columns 0-31); the gate warp runs a chunk ahead. ----
-            if (pw == 0 || pw == 5 || pw == 1) {
-                const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant of warps 4 / 9
-                const int t = row, s0 = 32 * half;         // warp 4: t 0-31, s 0-31; 9: 32-63, 32-63; 5: 32-63, 0-31
-                float gi[32];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(ps + C + s0 + i);
-                    gi[i] = x.x;
-                    gi[i + 1] = x.y;
-                    gi[i + 2] = x.z;
-                    gi[i + 3] = x.w;
-                }
-                const float f = sg_bg[t];
-                float v[32];
-                tmem_ld32(trow + T_G + 32 * half, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = (s0 + i < t) ? f * gi[i] * v[i] : 0.f;
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    *reinterpret_cast<float4*>(Lf + t * kLdF + s0 + 4 * q4) =
-                        make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-                if (pw != 1) {
-                    // the 16x16 diagonal block of row t (columns (lane & 16) .. +15 of this half)
-                    float* dst = Ld + (t >> 4) * 16 * 17 + (t & 15) * 17;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[i] = (lane & 16) ? v[16 + i] : v[i];
-                    __syncwarp();
+            //      0-31) and warp 9 (rows 32-63, columns 32-63) each take a whole diagonal 32-block of L and
+            //      invert it alone: two 16x16 forward substitutions and one merge, then its T operands;
+            //      the gate warp runs a chunk ahead. ----
+            if (pw == 0 || pw == 5) {
+                const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant: rows / columns 32 qw .. + 31
+                const int t = row, s0 = 32 * half;         // warp 4: t 0-31, s 0-31; warp 9: t 32-63, s 32-63
+                {
                     // lanes 0-15: column jc of block 2 qw; lanes 16-31: of block 2 qw + 1 (forward substitution,
                     // each dot product in four partial sums)
                     {
@@ -883,10 +922,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             tc_fence_before();
             mbar_arrive(bar_wready);
 
-            // ---- P = mask(q_t . k_s), once the chain's previous U''^T P^T is done ----
+            // ---- P = mask(q_t . k_s) from the Q rows of [K; Q] K^T, once the chain's previous U''^T P^T is done ----
             if (rd) {
                 if (j > 0 && !group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
                     break;
+                if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                tc_fence_after();
                 if (lq >= 2) {
                     float v[32];
                     tmem_ld32(trow + T_G + 32 * half, v);
@@ -904,8 +945,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         }
     } else if (lane == 0) {
         // ============================ MMA issue (warp 12, one lane) ============================
-        // Two streams, each in its own order: chain U_j, O1_j, St_j, O2_j and prep G_j, WU_j.  An item
-        // is issued once the mbarriers of its operands have fired; a stream ends after its last chunk.
+        // Two streams, each in its own order: prep G_j, WU_j (served first) and chain U_j, O1_j, St_j, O2_j.
+        // An item is issued once the mbarriers of its operands have fired; a stream ends after its last chunk.
         int jc = 0, sc = 0, jp = 0, sp = 0;
         bool chain_done = false, prep_done = false;
         uint64_t t_last = global_ns();
@@ -915,10 +956,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             bool progressed = false;
             if (!prep_done) {
                 const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
-                if (sp == 0) {
-                    if (mbar_test(bar_gin, jp & 1)) {
-                        tc_fence_after();
-                        // G = [K; Q] K^T
+                if (sp == 0 && mbar_test(bar_gin, jp & 1)) {
+                    tc_fence_after();
+                    if (rd) {
+                        // [K; Q] K^T (its Q rows give P)
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -926,32 +967,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         }
                         umma_commit(bar_g);
                         ++cnt[2];
-                        sp = 1;
-                        progressed = true;
                     }
+                    sp = 1;
+                    progressed = true;
                 }
-                if (sp == 1) {
-                    if (mbar_test(bar_wuin, jp & 1) && (jp == 0 || mbar_test(bar_ufree, (jp - 1) & 1))) {
-                        tc_fence_after();
-                        // W^T = K^T T1^T, U~^T = V^T T2^T
-                        const uint32_t inV = sbase + OFF_V;
+                if (sp == 1 && mbar_test(bar_wuin, jp & 1) && (jp == 0 || mbar_test(bar_ufree, (jp - 1) & 1))) {
+                    tc_fence_after();
+                    // W^T = K^T T1^T, U~^T = V^T T2^T
+                    const uint32_t inV = sbase + OFF_V;
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
-                            const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
-                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
-                            umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
-                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
-                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
-                        }
-                        umma_commit(bar_wu);
-                        ++cnt[3];
-                        progressed = true;
-                        if (ring[jp % kRing].last) prep_done = true;
-                        else {
-                            ++jp;
-                            sp = 0;
-                        }
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
+                        const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
+                        umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
+                        umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
+                        umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
+                        umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
+                    }
+                    umma_commit(bar_wu);
+                    ++cnt[3];
+                    progressed = true;
+                    if (ring[jp % kRing].last) prep_done = true;
+                    else {
+                        ++jp;
+                        sp = 0;
                     }
                 }
             }
