@@ -35,6 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import synth  # noqa: E402
@@ -304,6 +305,61 @@ def placement_report(N: int = 8192, M: int = 16, n_requests: int = 10000):
     return out
 
 
+def overlap_report(dev, reps: int = 5):
+    """Transfer / replay overlap ("Tail-Replay" notes page, section 2.5) on the 5 % replay workload:
+    768 (layer, head) scans, tail k = 1639 of m = 32768, replayed from zero.  The transfer is the
+    matched prefix's attention KV of an assumed 3:1 hybrid (8 attention layers, 8 KV heads x 128,
+    bf16): 32768 tokens x 8 x 2 x 8 x 128 x 2 B = 1 GiB from pinned host memory.  Times are medians of
+    CUDA-event spans on the compute stream."""
+    import hybrid_model_recurrent_gb300 as gdn
+    k_tail, H = 1639, 768
+    w = synth.Workload("replay5-tail", [k_tail], H, 128, 128, torch.bfloat16, torch.bfloat16, 0.97, 1.0,
+                       "uniform", seed=0)
+    inp = synth.make_inputs(w, device=dev)
+    cu, m = w.cu_seqlens, [k_tail]
+    kv_bytes = 32768 * 8 * 2 * 8 * 128 * 2
+    kv_h = torch.empty(kv_bytes, dtype=torch.uint8).pin_memory()
+    kv_d = torch.empty(kv_bytes, dtype=torch.uint8, device=dev)
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    S_hat = torch.empty((1, H, 128, 128), dtype=torch.float32, device=dev)
+    ws = gdn.workspace(dev)
+
+    def replay():
+        gdn.gdn_tail_replay(None, inp.k, inp.v, inp.alpha, inp.beta, cu, m, 1, 1, S_hat=S_hat, ws=ws)
+
+    def transfer():
+        kv_d.copy_(kv_h, non_blocking=True)
+
+    def serial():
+        transfer()
+        replay()
+
+    def overlapped():
+        gdn.gdn_tail_replay_overlap(None, inp.k, inp.v, inp.alpha, inp.beta, cu, m, 1, 1, kv_h, kv_d,
+                                    copy_stream=copy, S_hat=S_hat, ws=ws)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(comp)
+            fn()
+            e1.record(comp)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    t_rep, t_kv, t_ser, t_ovl = timed(replay), timed(transfer), timed(serial), timed(overlapped)
+    return {"workload": "768 scans x tail 1639 (5 % of 32768), state only; KV 1 GiB pinned H2D",
+            "unit": "ms", "T_replay": t_rep, "T_KV": t_kv, "T_serial": t_ser, "T_overlap": t_ovl,
+            "model_max": max(t_rep, t_kv), "model_sum": t_rep + t_kv,
+            "kv_GBps": kv_bytes / (t_kv * 1e-3) / 1e9,
+            "replay_Mtok_head_per_s": k_tail * H / (t_rep * 1e-3) / 1e6}
+
+
 def cpu_baseline(w: synth.Workload):
     threads = os.cpu_count() or 1
     pairs = [(b, h) for b in range(w.B) for h in range(w.H)][: 2 * threads]
@@ -460,6 +516,7 @@ def run_ours(args, ws, rank, local):
             "states_per_s": sum(len(c) for c in step.ck) * w.H * args.steps / slowest,
             "cpu_baseline": base,
             "placement": placement_report(),
+            "replay_overlap": overlap_report(dev),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -72,6 +72,10 @@ def lib():
                                           vp]
             L.gdn_replay_plan.argtypes = [i64, i32, i32, pi64, pi64]
             L.gdn_select_ckpt.argtypes = [pi64, i32, i64, pi32]
+            L.gdn_tail_replay_k.argtypes = [P, vp, vp, vp, vp, vp, pi64, pi64, vp, vp, vp, vp, vp, sz, vp]
+            L.gdn_tail_replay_overlap.argtypes = [P, vp, vp, vp, vp, vp, pi64, i32, i32, vp, vp, vp, vp, pi64, pi64,
+                                                  vp, vp, sz, vp, sz, vp, vp]
+            L.gdn_adaptive_replay_plan.argtypes = [P, vp, pi64, ctypes.c_float, i32, i32, pi64, pi32]
             L.gdn_ckpt_placement.argtypes = [pi64, i64, i32, ctypes.c_int, ctypes.c_uint64, i64, pi64, pi32, pi64]
             L.gdn_expected_recompute.argtypes = [pi64, i64, pi64, i32, pi64]
             L.gdn_workspace_size.argtypes = []
@@ -336,3 +340,81 @@ def gdn_tail_replay(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int,
     _check(rc, "gdn_tail_replay")
     return {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o, "a": a_out.tolist(),
             "k": k_out.tolist()}
+
+
+def _replay_buffers(k, v, B, S_a, readout, out_dtype, S_hat, S_exact, o):
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    out_dtype = out_dtype or k.dtype
+    if S_hat is None:
+        S_hat = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    if S_a is not None and S_exact is None:
+        S_exact = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    if readout and o is None:
+        o = torch.zeros((T, H, dv), dtype=out_dtype, device=dev)
+    if not readout:
+        o = None
+    return T, H, dk, dv, dev, out_dtype, S_hat, S_exact, o
+
+
+def gdn_tail_replay_k(q, k, v, alpha, beta, cu_seqlens, m, k_replay, *, S_a=None, readout: bool = False,
+                      out_dtype: Optional[torch.dtype] = None, S_hat=None, S_exact=None, o=None, stream=None,
+                      ws: Optional[torch.Tensor] = None, algo: str = "auto"):
+    """Tail replay of the k_replay[b] tokens before m[b] of every sequence (zero initial state).
+
+    Returns dict(S_hat, S_exact or None, o or None)."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    T, H, dk, dv, dev, out_dtype, S_hat, S_exact, o = _replay_buffers(k, v, B, S_a, readout, out_dtype, S_hat,
+                                                                      S_exact, o)
+    ws = ws if ws is not None else workspace(dev)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
+    rc = lib().gdn_tail_replay_k(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
+                                 _ptr(beta), _p64(_i64(m)), _p64(_i64(k_replay)), _ptr(S_a), _ptr(S_hat),
+                                 _ptr(S_exact if S_a is not None else None), _ptr(o), _ptr(ws), ws.numel(),
+                                 _stream(stream, dev))
+    _check(rc, "gdn_tail_replay_k")
+    return {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o}
+
+
+def gdn_tail_replay_overlap(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int, kv_host, kv_dev, *,
+                            copy_stream, S_a=None, readout: bool = False, out_dtype: Optional[torch.dtype] = None,
+                            S_hat=None, S_exact=None, o=None, stream=None, ws: Optional[torch.Tensor] = None,
+                            algo: str = "auto"):
+    """gdn_tail_replay with kv_host (pinned) copied into kv_dev on copy_stream beside the replay;
+    `stream` waits for the copy afterwards.  Returns the gdn_tail_replay dict."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    T, H, dk, dv, dev, out_dtype, S_hat, S_exact, o = _replay_buffers(k, v, B, S_a, readout, out_dtype, S_hat,
+                                                                      S_exact, o)
+    nbytes = kv_host.numel() * kv_host.element_size()
+    if kv_dev.numel() * kv_dev.element_size() != nbytes:
+        raise ValueError("kv_host and kv_dev sizes differ")
+    a_out = np.zeros(B, dtype=np.int64)
+    k_out = np.zeros(B, dtype=np.int64)
+    ws = ws if ws is not None else workspace(dev)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
+    rc = lib().gdn_tail_replay_overlap(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v),
+                                       _ptr(alpha), _ptr(beta), _p64(_i64(m)), r_num, r_den, _ptr(S_a), _ptr(S_hat),
+                                       _ptr(S_exact if S_a is not None else None), _ptr(o), _p64(a_out),
+                                       _p64(k_out), ctypes.c_void_p(kv_host.data_ptr()),
+                                       ctypes.c_void_p(kv_dev.data_ptr()), nbytes, _ptr(ws), ws.numel(),
+                                       _stream(stream, dev), _stream(copy_stream, dev))
+    _check(rc, "gdn_tail_replay_overlap")
+    return {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o, "a": a_out.tolist(),
+            "k": k_out.tolist()}
+
+
+def gdn_adaptive_replay_plan(alpha, cu_seqlens, m, eps: float, rmax_num: int, rmax_den: int, H: int,
+                             d_k: int = 128, d_v: int = 128):
+    """Per-sequence tail length from the gates (see the header): (k list, exact-recovery flags)."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    k_out = np.zeros(B, dtype=np.int64)
+    ex = np.zeros(B, dtype=np.int32)
+    pr = _problem(cu, H, d_k, d_v, torch.bfloat16, torch.bfloat16)
+    rc = lib().gdn_adaptive_replay_plan(ctypes.byref(pr), _ptr(alpha), _p64(_i64(m)), ctypes.c_float(eps),
+                                        rmax_num, rmax_den, _p64(k_out), ex.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    _check(rc, "gdn_adaptive_replay_plan")
+    return k_out.tolist(), ex.tolist()

@@ -449,42 +449,186 @@ GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, 
 // ---------------------------------------------------------------------------------------
 // Tail-Replay
 // ---------------------------------------------------------------------------------------
-GDN_EXPORT gdn_status gdn_tail_replay(const gdn_problem* p, const void* q, const void* k, const void* v,
-                                      const float* alpha, const float* beta, const int64_t* m, int32_t r_num,
-                                      int32_t r_den, const float* S_a, float* S_hat, float* S_exact, void* o,
-                                      int64_t* a_out, int64_t* k_out, void* workspace, size_t ws_bytes,
-                                      gdn_stream_t stream) {
+// Tail replay with a given tail length k_b per sequence (rows [m_b - k_b, m_b)): every check and the job
+// table, nothing enqueued.
+static gdn_status replay_prepare(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                 const float* alpha, const float* beta, const int64_t* m, const int64_t* kv,
+                                 const float* S_a, float* S_hat, float* S_exact, void* o, void* workspace,
+                                 size_t ws_bytes, std::vector<HostJob>& jobs, LaunchSpec& L) {
     std::vector<int64_t> lens;
     gdn_status st = check_problem(p, lens);
     if (st != GDN_OK) return st;
-    if (!m || !S_hat || !aligned(S_hat, 16)) return GDN_ERR_INVALID_ARG;
+    if (!m || !kv || !S_hat || !aligned(S_hat, 16)) return GDN_ERR_INVALID_ARG;
     if ((S_a == nullptr) != (S_exact == nullptr)) return GDN_ERR_INVALID_ARG;
     if (S_a && (!aligned(S_a, 16) || !aligned(S_exact, 16))) return GDN_ERR_INVALID_ARG;
     if (o && !aligned(o, p->out_dtype == GDN_BF16 ? 2 : 4)) return GDN_ERR_INVALID_ARG;
     if ((st = check_workspace(workspace, ws_bytes)) != GDN_OK) return st;
     const int B = p->num_seqs;
     const size_t D = (size_t)p->num_heads * p->d_v * p->d_k;
-    std::vector<HostJob> jobs(B);
-    std::vector<int64_t> av(B), kv(B);
+    jobs.assign(B, HostJob{});
     int64_t total = 0;
     for (int b = 0; b < B; ++b) {
-        if (m[b] < 0 || m[b] > lens[b]) return GDN_ERR_INVALID_ARG;
-        if (gdn_replay_plan(m[b], r_num, r_den, &av[b], &kv[b]) != GDN_OK) return GDN_ERR_INVALID_ARG;
+        if (m[b] < 0 || m[b] > lens[b] || kv[b] < 0 || kv[b] > m[b]) return GDN_ERR_INVALID_ARG;
+        const int64_t a = m[b] - kv[b];
         total += kv[b];
         gdn::Job& j = jobs[b].job;
         std::memset(&j, 0, sizeof(j));
-        j.tok_begin = p->cu_seqlens[b] + av[b];
+        j.tok_begin = p->cu_seqlens[b] + a;
         j.len = (int32_t)kv[b];
-        j.o_row_begin = o ? p->cu_seqlens[b] + av[b] : -1;
+        j.o_row_begin = o ? p->cu_seqlens[b] + a : -1;
         j.s0 = nullptr;
         j.s0_twin = S_a ? S_a + (size_t)b * D : nullptr;
         j.s_final = S_hat + (size_t)b * D;
         j.s_final_twin = S_exact ? S_exact + (size_t)b * D : nullptr;
     }
     if ((st = check_streams(p, q, k, v, alpha, beta, o != nullptr, total > 0)) != GDN_OK) return st;
-    if (a_out) std::copy(av.begin(), av.end(), a_out);
-    if (k_out) std::copy(kv.begin(), kv.end(), k_out);
-    LaunchSpec L{p, q, k, v, alpha, beta, o, nullptr, static_cast<unsigned int*>(workspace), o != nullptr,
-                 S_a != nullptr};
-    return run_jobs(L, jobs, (cudaStream_t)stream);
+    L = LaunchSpec{p, q, k, v, alpha, beta, o, nullptr, static_cast<unsigned int*>(workspace), o != nullptr,
+                   S_a != nullptr};
+    return GDN_OK;
+}
+
+static gdn_status replay_k(const gdn_problem* p, const void* q, const void* k, const void* v, const float* alpha,
+                           const float* beta, const int64_t* m, const int64_t* kv, const float* S_a, float* S_hat,
+                           float* S_exact, void* o, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    std::vector<HostJob> jobs;
+    LaunchSpec L{};
+    gdn_status st = replay_prepare(p, q, k, v, alpha, beta, m, kv, S_a, S_hat, S_exact, o, workspace, ws_bytes,
+                                   jobs, L);
+    if (st != GDN_OK) return st;
+    return run_jobs(L, jobs, stream);
+}
+
+static gdn_status plan_all(int B, const int64_t* m, int32_t r_num, int32_t r_den, std::vector<int64_t>& av,
+                           std::vector<int64_t>& kv) {
+    if (B < 1 || !m) return GDN_ERR_INVALID_ARG;
+    av.resize(B);
+    kv.resize(B);
+    for (int b = 0; b < B; ++b)
+        if (gdn_replay_plan(m[b], r_num, r_den, &av[b], &kv[b]) != GDN_OK) return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+GDN_EXPORT gdn_status gdn_tail_replay(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                      const float* alpha, const float* beta, const int64_t* m, int32_t r_num,
+                                      int32_t r_den, const float* S_a, float* S_hat, float* S_exact, void* o,
+                                      int64_t* a_out, int64_t* k_out, void* workspace, size_t ws_bytes,
+                                      gdn_stream_t stream) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    std::vector<int64_t> av, kv;
+    gdn_status st = plan_all(p->num_seqs, m, r_num, r_den, av, kv);
+    if (st != GDN_OK) return st;
+    st = replay_k(p, q, k, v, alpha, beta, m, kv.data(), S_a, S_hat, S_exact, o, workspace, ws_bytes,
+                  (cudaStream_t)stream);
+    if (st == GDN_OK || st == GDN_ERR_CUDA) {
+        if (a_out) std::copy(av.begin(), av.end(), a_out);
+        if (k_out) std::copy(kv.begin(), kv.end(), k_out);
+    }
+    return st;
+}
+
+GDN_EXPORT gdn_status gdn_tail_replay_k(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                        const float* alpha, const float* beta, const int64_t* m,
+                                        const int64_t* k_replay, const float* S_a, float* S_hat, float* S_exact,
+                                        void* o, void* workspace, size_t ws_bytes, gdn_stream_t stream) {
+    return replay_k(p, q, k, v, alpha, beta, m, k_replay, S_a, S_hat, S_exact, o, workspace, ws_bytes,
+                    (cudaStream_t)stream);
+}
+
+GDN_EXPORT gdn_status gdn_tail_replay_overlap(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                              const float* alpha, const float* beta, const int64_t* m,
+                                              int32_t r_num, int32_t r_den, const float* S_a, float* S_hat,
+                                              float* S_exact, void* o, int64_t* a_out, int64_t* k_out,
+                                              const void* kv_host, void* kv_dev, size_t kv_bytes, void* workspace,
+                                              size_t ws_bytes, gdn_stream_t stream, gdn_stream_t copy_stream) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    if (kv_bytes > 0 && (!kv_host || !kv_dev)) return GDN_ERR_INVALID_ARG;
+    std::vector<int64_t> av, kv;
+    gdn_status st = plan_all(p->num_seqs, m, r_num, r_den, av, kv);
+    if (st != GDN_OK) return st;
+    // every check of the replay before anything is enqueued
+    std::vector<HostJob> jobs;
+    LaunchSpec L{};
+    if ((st = replay_prepare(p, q, k, v, alpha, beta, m, kv.data(), S_a, S_hat, S_exact, o, workspace, ws_bytes, jobs,
+                             L)) != GDN_OK)
+        return st;
+    const cudaStream_t cs = (cudaStream_t)stream, xs = (cudaStream_t)copy_stream;
+    cudaEvent_t before = nullptr, copied = nullptr;
+    if (kv_bytes > 0) {
+        if (cudaEventCreateWithFlags(&before, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&copied, cudaEventDisableTiming) != cudaSuccess) {
+            if (before) cudaEventDestroy(before);
+            return GDN_ERR_CUDA;
+        }
+        // the copy waits for the caller's earlier work on `stream` (which may still use kv_dev), then runs
+        // beside the replay
+        bool ok = cudaEventRecord(before, cs) == cudaSuccess && cudaStreamWaitEvent(xs, before, 0) == cudaSuccess &&
+                  cudaMemcpyAsync(kv_dev, kv_host, kv_bytes, cudaMemcpyHostToDevice, xs) == cudaSuccess &&
+                  cudaEventRecord(copied, xs) == cudaSuccess;
+        if (!ok) {
+            cudaEventDestroy(before);
+            cudaEventDestroy(copied);
+            return GDN_ERR_CUDA;
+        }
+    }
+    st = run_jobs(L, jobs, cs);
+    if (kv_bytes > 0) {
+        // later work on `stream` (the new suffix) sees the copied KV
+        if (cudaStreamWaitEvent(cs, copied, 0) != cudaSuccess && st == GDN_OK) st = GDN_ERR_CUDA;
+        cudaEventDestroy(before);
+        cudaEventDestroy(copied);
+    }
+    if (st == GDN_OK || st == GDN_ERR_CUDA) {
+        if (a_out) std::copy(av.begin(), av.end(), a_out);
+        if (k_out) std::copy(kv.begin(), kv.end(), k_out);
+    }
+    return st;
+}
+
+GDN_EXPORT gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, const int64_t* m,
+                                               float eps, int32_t rmax_num, int32_t rmax_den, int64_t* k_out,
+                                               int32_t* exact_out) {
+    std::vector<int64_t> lens;
+    gdn_status st = check_problem(p, lens);
+    if (st != GDN_OK) return st;
+    if (!alpha || !m || !k_out || !exact_out || !(eps >= 0.f) || !(eps < 1.f)) return GDN_ERR_INVALID_ARG;
+    const int B = p->num_seqs, H = p->num_heads;
+    std::vector<int64_t> av, kmax;
+    if ((st = plan_all(B, m, rmax_num, rmax_den, av, kmax)) != GDN_OK) return st;
+    for (int b = 0; b < B; ++b)
+        if (m[b] > lens[b]) return GDN_ERR_INVALID_ARG;
+    std::vector<float> tail;
+    for (int b = 0; b < B; ++b) {
+        const int64_t K = kmax[b];
+        int64_t need = 0;
+        bool reached = true;
+        if (K > 0) {
+            tail.resize((size_t)K * H);
+            // gates of rows [m_b - K, m_b): the budget's tail of every head
+            if (cudaMemcpy(tail.data(), alpha + (size_t)(p->cu_seqlens[b] + m[b] - K) * H, sizeof(float) * tail.size(),
+                           cudaMemcpyDeviceToHost) != cudaSuccess)
+                return GDN_ERR_CUDA;
+            for (int h = 0; h < H; ++h) {
+                // smallest k with alpha_m * alpha_{m-1} * ... * alpha_{m-k+1} <= eps (fp32, newest gate first)
+                float prod = 1.f;
+                int64_t kh = -1;
+                for (int64_t i = 1; i <= K; ++i) {
+                    prod *= tail[(size_t)(K - i) * H + h];
+                    if (prod <= eps) {
+                        kh = i;
+                        break;
+                    }
+                }
+                if (kh < 0) {
+                    reached = false;
+                    kh = K;
+                }
+                need = std::max(need, kh);
+            }
+        } else {
+            reached = m[b] == 0;   // an empty budget recovers only an empty prefix
+        }
+        k_out[b] = need;
+        exact_out[b] = reached ? 0 : 1;
+    }
+    return GDN_OK;
 }

@@ -182,6 +182,59 @@ gdn_status gdn_tail_replay(const gdn_problem* p, const void* q, const void* k, c
                            gdn_stream_t stream);
 
 /*
+ * Tail replay with a caller-chosen tail length per sequence: rows [m_b - k_b, m_b)
+ * of sequence b from a zero state (and the exact twin from S_a when given).  Same
+ * buffers and rules as gdn_tail_replay; k_replay host int64 [B] with
+ * 0 <= k_b <= m_b (e.g. from gdn_adaptive_replay_plan).
+ */
+gdn_status gdn_tail_replay_k(const gdn_problem* p, const void* q, const void* k, const void* v,
+                             const float* alpha, const float* beta, const int64_t* m, const int64_t* k_replay,
+                             const float* S_a, float* S_hat, float* S_exact, void* o, void* workspace,
+                             size_t ws_bytes, gdn_stream_t stream);
+
+/*
+ * Tail replay with the prefix's cached attention KV copied to the device at the
+ * same time ("Tail-Replay" notes page, section 2.5, transfer / replay overlap:
+ * the replay needs only the tail's inputs, not the KV, so the two run on
+ * different streams and join before the new suffix is processed; the page's
+ * latency model T_overlap ~ max(T_KV, T_replay) + T_other against
+ * T_serial ~ T_KV + T_replay + T_other).
+ *  Arguments as gdn_tail_replay, plus:
+ *  kv_host     host buffer of kv_bytes (pinned memory for a truly asynchronous copy)
+ *  kv_dev      device buffer of kv_bytes
+ *  copy_stream stream for the copy.  The copy starts after the work already
+ *              enqueued on `stream` (which may still use kv_dev), runs beside the
+ *              replay, and `stream` waits for it after the replay, so work enqueued
+ *              on `stream` afterwards sees the copied KV.  kv_bytes = 0 copies nothing.
+ *  Every argument is checked before anything is enqueued (GDN_ERR_INVALID_ARG);
+ *  GDN_ERR_CUDA if enqueueing the copy or its events fails.
+ */
+gdn_status gdn_tail_replay_overlap(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                   const float* alpha, const float* beta, const int64_t* m, int32_t r_num,
+                                   int32_t r_den, const float* S_a, float* S_hat, float* S_exact, void* o,
+                                   int64_t* a_out, int64_t* k_out, const void* kv_host, void* kv_dev,
+                                   size_t kv_bytes, void* workspace, size_t ws_bytes, gdn_stream_t stream,
+                                   gdn_stream_t copy_stream);
+
+/*
+ * Adaptive tail length per request ("Tail-Replay" notes page, section 5, the
+ * proposed extension: shorter tails where the state forgets fast, longer ones or
+ * exact recovery where it does not).  With unit keys and beta in [0, 2] the
+ * replay error obeys ||E_m||_F <= (alpha_{a+1} ... alpha_m) ||S_a||_F (section 2.3),
+ * so for each sequence b: k_b = the least k <= ceil(rmax_num m_b / rmax_den) with
+ * alpha_m alpha_{m-1} ... alpha_{m-k+1} <= eps for every head (the product taken in
+ * fp32, newest gate first), and exact_out[b] = 0; when the budget is too short for
+ * some head, k_b is the budget and exact_out[b] = 1 (recover that request exactly,
+ * e.g. from a checkpoint).
+ *  alpha     device [T, H] fp32 (only the budget's tail rows are read; copied to
+ *            the host, so the call synchronises with the device)
+ *  m         host int64 [B]; eps in [0, 1); rmax_num / rmax_den as in gdn_replay_plan
+ *  k_out     host int64 [B]; exact_out host int32 [B]
+ */
+gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, const int64_t* m, float eps,
+                                    int32_t rmax_num, int32_t rmax_den, int64_t* k_out, int32_t* exact_out);
+
+/*
  * Prefill with sparse checkpoints for callers that cannot allocate device memory.
  * (No counterpart on the pages: this is a calling convention of this library.)
  *

@@ -176,3 +176,38 @@ def run_many(jobs: List[Callable], threads: Optional[int] = None):
         return [j() for j in jobs]
     with ThreadPoolExecutor(max_workers=threads) as ex:
         return list(ex.map(lambda f: f(), jobs))
+
+
+def adaptive_replay_plan(alpha, cu_seqlens: Sequence[int], m: Sequence[int], eps: float, rmax_num: int,
+                         rmax_den: int):
+    """Adaptive tail length per request ("Tail-Replay" notes page, section 5, the proposed extension;
+    the bound of section 2.3): k_b = the least k <= ceil(rmax m_b) such that the product of the last
+    k gates is <= eps for every head, taken in fp32 with the newest gate first; when the budget is too
+    short for some head, k_b = the budget and the request is flagged for exact recovery.
+
+    alpha: [T, H] float32 (numpy or torch on the CPU).  Returns (k list, exact flags)."""
+    a = np.asarray(alpha.cpu().numpy() if hasattr(alpha, "cpu") else alpha, dtype=np.float32)
+    H = a.shape[1]
+    e = np.float32(eps)
+    ks, flags = [], []
+    for b in range(len(cu_seqlens) - 1):
+        _, K = replay_plan(int(m[b]), rmax_num, rmax_den)
+        need, reached = 0, True
+        if K == 0:
+            reached = int(m[b]) == 0
+        for h in range(H):
+            if K == 0:
+                break
+            prod = np.float32(1.0)
+            kh = None
+            for i in range(1, K + 1):
+                prod = np.float32(prod * a[cu_seqlens[b] + int(m[b]) - i, h])
+                if prod <= e:
+                    kh = i
+                    break
+            if kh is None:
+                reached, kh = False, K
+            need = max(need, kh)
+        ks.append(need)
+        flags.append(0 if reached else 1)
+    return ks, flags

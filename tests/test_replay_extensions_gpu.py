@@ -1,0 +1,145 @@
+"""Replay extensions on the GPU, through the C ABI ("Tail-Replay" notes page):
+* gdn_tail_replay_k (caller-chosen tail per request) and gdn_adaptive_replay_plan (section 5, the
+  proposed extension) against the oracle;
+* gdn_tail_replay_overlap (section 2.5, transfer / replay overlap): identical states, the copy
+  delivered, and the overlapped time close to the longer of the two instead of their sum.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hybrid_model_recurrent_gb300 as gdn
+import oracle
+import synth
+from parity_util import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gdn.build()
+    gdn.lib()
+    gdn.clear_status(DEV)
+    yield
+    assert gdn.read_status(DEV) == gdn.GDN_OK, "a kernel reported a device-side timeout"
+
+
+def _inputs(seed, lens, H, d, dtype, a_lo, a_hi):
+    w = synth.Workload("ext", list(lens), H, d, d, dtype, dtype, a_lo, a_hi, "uniform", seed=seed)
+    return w, synth.make_inputs(w)
+
+
+def _dev(inp):
+    return synth.Inputs(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.alpha.to(DEV), inp.beta.to(DEV))
+
+
+@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+def test_replay_k_matches_r_based_replay_and_oracle(algo):
+    lens = [300, 129, 64]
+    H = 2
+    w, inp = _inputs(81, lens, H, 128, torch.bfloat16, 0.9, 1.0)
+    d = _dev(inp)
+    cu = w.cu_seqlens
+    m = [300, 100, 64]
+    S_a = synth.state(3, w.B * H, 128, 128, 1.0).view(w.B, H, 128, 128)
+    a = gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 10, S_a=S_a.to(DEV), algo=algo)
+    b = gdn.gdn_tail_replay_k(d.q, d.k, d.v, d.alpha, d.beta, cu, m, a["k"], S_a=S_a.to(DEV), algo=algo)
+    torch.cuda.synchronize()
+    assert torch.equal(a["S_hat"], b["S_hat"]) and torch.equal(a["S_exact"], b["S_exact"])
+    ks = [7, 100, 0]
+    c = gdn.gdn_tail_replay_k(d.q, d.k, d.v, d.alpha, d.beta, cu, m, ks, algo=algo)
+    torch.cuda.synchronize()
+    for s in range(w.B):
+        sl = slice(cu[s], cu[s + 1])
+        for h in range(H):
+            ref = oracle.tail_replay(inp.k[sl, h], inp.v[sl, h], inp.alpha[sl, h], inp.beta[sl, h], m[s], ks[s],
+                                     max(m[s], 1))
+            assert_close(c["S_hat"][s, h], ref["S_hat"], f"replay_k s={s} h={h}")
+
+
+def test_adaptive_plan_matches_oracle_and_meets_the_bound():
+    lens = [1200, 700, 2000]
+    H = 4
+    w, inp = _inputs(83, lens, H, 128, torch.bfloat16, 0.9, 1.0)
+    # heads that forget at different rates: head 0 fast, head 3 almost not at all
+    alpha = inp.alpha.clone()
+    alpha[:, 0] = alpha[:, 0] * 0.9
+    alpha[:, 3] = torch.clamp(0.999 + 0.001 * alpha[:, 3], max=1.0)
+    inp = synth.Inputs(inp.q, inp.k, inp.v, alpha, inp.beta)
+    d = _dev(inp)
+    cu = w.cu_seqlens
+    m = [1200, 650, 2000]
+    for eps, rmax in ((1e-2, (1, 5)), (1e-4, (1, 2)), (0.3, (1, 20))):
+        ks, ex = gdn.gdn_adaptive_replay_plan(d.alpha, cu, m, eps, *rmax, H=H)
+        ks_o, ex_o = oracle.adaptive_replay_plan(alpha, cu, m, eps, *rmax)
+        assert (ks, ex) == (ks_o, ex_o), (eps, rmax)
+    # replay the planned tails (exact twin from a seeded S_a) and check ||E|| <= eps ||S_a|| where met
+    eps, rmax = 1e-2, (1, 1)
+    ks, ex = gdn.gdn_adaptive_replay_plan(d.alpha, cu, m, eps, *rmax, H=H)
+    S_a = synth.state(5, w.B * H, 128, 128, 1.0).view(w.B, H, 128, 128)
+    r = gdn.gdn_tail_replay_k(d.q, d.k, d.v, d.alpha, d.beta, cu, m, ks, S_a=S_a.to(DEV))
+    torch.cuda.synchronize()
+    E = (r["S_exact"] - r["S_hat"]).double().cpu()
+    for s in range(w.B):
+        if ex[s]:
+            continue
+        for h in range(H):
+            bound = eps * float(torch.linalg.norm(S_a[s, h].double()))
+            assert float(torch.linalg.norm(E[s, h])) <= bound * (1 + 1e-3) + 1e-5, (s, h)
+
+
+def _timed(stream, fn, reps=5):
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return float(np.median(ts))
+
+
+def test_overlap_gives_identical_states_and_hides_the_shorter_leg():
+    H, T = 256, 1024                       # 256 (layer, head) scans, a 1024-token tail each
+    w, inp = _inputs(85, [T], H, 128, torch.bfloat16, 0.97, 1.0)
+    d = _dev(inp)
+    cu, m = w.cu_seqlens, [T]
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ref = gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 1)
+    torch.cuda.synchronize()
+    t_rep = _timed(comp, lambda: gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 1))
+    # size the transfer to take about as long as the replay
+    probe_h = torch.empty(64 << 20, dtype=torch.uint8).pin_memory()
+    probe_d = torch.empty_like(probe_h, device=DEV)
+    t_probe = _timed(comp, lambda: probe_d.copy_(probe_h, non_blocking=True))
+    nbytes = int(min(max(probe_h.numel() * t_rep / t_probe, 1 << 20), 2 << 30)) // 4096 * 4096
+    kv_h = torch.randint(0, 255, (nbytes,), dtype=torch.uint8).pin_memory()
+    kv_d = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    t_kv = _timed(comp, lambda: kv_d.copy_(kv_h, non_blocking=True))
+
+    def serial():
+        kv_d.copy_(kv_h, non_blocking=True)
+        gdn.gdn_tail_replay(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 1)
+
+    def overlapped():
+        return gdn.gdn_tail_replay_overlap(d.q, d.k, d.v, d.alpha, d.beta, cu, m, 1, 1, kv_h, kv_d,
+                                           copy_stream=copy)
+
+    kv_d.zero_()
+    r = overlapped()
+    torch.cuda.synchronize()
+    assert torch.equal(r["S_hat"], ref["S_hat"]), "the overlapped replay must not change the states"
+    assert torch.equal(kv_d.cpu(), kv_h), "the copy was not delivered"
+    t_ser = _timed(comp, serial)
+    t_ovl = _timed(comp, overlapped)
+    longer, shorter = max(t_kv, t_rep), min(t_kv, t_rep)
+    print(f"T_KV {t_kv:.3f} ms, T_replay {t_rep:.3f} ms, serial {t_ser:.3f} ms, overlapped {t_ovl:.3f} ms")
+    assert shorter > 0.3 * longer, "the two legs should be comparable for this check"
+    assert t_ovl < t_ser - 0.5 * shorter, "the overlap hides less than half of the shorter leg"
+    assert t_ovl > 0.9 * longer, "faster than the longer leg alone: the timing is not what it seems"
