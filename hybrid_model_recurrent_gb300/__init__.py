@@ -36,6 +36,11 @@ _lib = None
 _workspaces: Dict[int, torch.Tensor] = {}
 
 
+class _Group(ctypes.Structure):
+    _fields_ = [("layers", ctypes.c_int32), ("heads", ctypes.c_int32), ("d_model", ctypes.c_int32),
+                ("d_head", ctypes.c_int32)]
+
+
 class GdnError(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {status_string(status)} ({status})")
@@ -76,6 +81,10 @@ def lib():
             L.gdn_tail_replay_overlap.argtypes = [P, vp, vp, vp, vp, vp, pi64, i32, i32, vp, vp, vp, vp, pi64, pi64,
                                                   vp, vp, sz, vp, sz, vp, vp]
             L.gdn_adaptive_replay_plan.argtypes = [P, vp, pi64, ctypes.c_float, i32, i32, pi64, pi32]
+            G = ctypes.POINTER(_Group)
+            L.gdn_group_scratch_bytes.argtypes = [G, i64]
+            L.gdn_group_scratch_bytes.restype = sz
+            L.gdn_group_replay.argtypes = [G, vp, i64, i32, i32, vp, vp, vp, pi64, pi64, vp, sz, vp, sz, vp]
             L.gdn_ckpt_placement.argtypes = [pi64, i64, i32, ctypes.c_int, ctypes.c_uint64, i64, pi64, pi32, pi64]
             L.gdn_expected_recompute.argtypes = [pi64, i64, pi64, i32, pi64]
             L.gdn_workspace_size.argtypes = []
@@ -404,6 +413,27 @@ def gdn_tail_replay_overlap(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_d
     _check(rc, "gdn_tail_replay_overlap")
     return {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o, "a": a_out.tolist(),
             "k": k_out.tolist()}
+
+
+def gdn_group_replay(h, weights, layers: int, heads: int, d_model: int, d_head: int, m: int, r_num: int,
+                     r_den: int, *, exact: bool = True, stream=None, ws: Optional[torch.Tensor] = None):
+    """In-group chained replay of one request (see the header).  h [m, d_model] fp32 on the GPU,
+    weights flat fp32 on the GPU.  Returns dict(S_hat [layers, heads, d_head, d_head], S_exact or None, a, k)."""
+    dev = h.device
+    g = _Group(layers, heads, d_model, d_head)
+    a_o, k_o = ctypes.c_int64(), ctypes.c_int64()
+    _, kk = gdn_replay_plan(m, r_num, r_den)
+    rows = m if exact else kk
+    nbytes = lib().gdn_group_scratch_bytes(ctypes.byref(g), rows)
+    scratch = torch.empty(max(int(nbytes) // 4, 4), dtype=torch.float32, device=dev)
+    S_hat = torch.empty((layers, heads, d_head, d_head), dtype=torch.float32, device=dev)
+    S_exact = torch.empty_like(S_hat) if exact else None
+    ws = ws if ws is not None else workspace(dev)
+    rc = lib().gdn_group_replay(ctypes.byref(g), _ptr(h), m, r_num, r_den, _ptr(weights), _ptr(S_hat), _ptr(S_exact),
+                                ctypes.byref(a_o), ctypes.byref(k_o), _ptr(scratch), scratch.numel() * 4, _ptr(ws),
+                                ws.numel(), _stream(stream, dev))
+    _check(rc, "gdn_group_replay")
+    return {"S_hat": S_hat, "S_exact": S_exact, "a": a_o.value, "k": k_o.value}
 
 
 def gdn_adaptive_replay_plan(alpha, cu_seqlens, m, eps: float, rmax_num: int, rmax_den: int, H: int,

@@ -14,6 +14,7 @@
 #include "../../include/gdn_scan.h"
 #include "gdn_chunk.cuh"
 #include "gdn_chunk_tc.cuh"
+#include "gdn_group.cuh"
 #include "gdn_kernel.cuh"
 
 #define GDN_EXPORT extern "C" __attribute__((visibility("default")))
@@ -631,4 +632,103 @@ GDN_EXPORT gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float
         exact_out[b] = reached ? 0 : 1;
     }
     return GDN_OK;
+}
+
+// ------------------------------------------------------------------------------------
+// In-group chained replay ("Tail-Replay" notes page, section 2.2 step 3, section 2.4)
+// ------------------------------------------------------------------------------------
+namespace {
+
+size_t group_row_floats(const gdn_group* g) {
+    return 2 * (size_t)g->d_model + 4 * (size_t)g->heads * g->d_head + 2 * (size_t)g->heads;
+}
+size_t group_layer_floats(const gdn_group* g) {
+    return (4 * (size_t)g->heads * g->d_head + 2 * (size_t)g->heads) * (size_t)g->d_model;
+}
+bool group_ok(const gdn_group* g) {
+    return g && g->layers >= 1 && g->layers <= 64 && g->heads >= 1 && g->heads <= 1024 && g->d_model >= 1 &&
+           g->d_model <= 8192 && (g->d_head == 32 || g->d_head == 64 || g->d_head == 128) &&
+           (int64_t)g->heads * g->d_head <= 8192;
+}
+
+// One chain through the group over `rows` input rows: per layer project, scan from a zero state (readout
+// except after the last layer), mix into the next layer's input.
+gdn_status group_chain(const gdn_group* g, const float* h_in, int64_t rows, const float* weights, float* S_out,
+                       float* scratch, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    const int Dm = g->d_model, H = g->heads, d = g->d_head, Hd = H * d;
+    float* hA = scratch;
+    float* hB = hA + (size_t)rows * Dm;
+    float* q = hB + (size_t)rows * Dm;
+    float* k = q + (size_t)rows * Hd;
+    float* v = k + (size_t)rows * Hd;
+    float* o = v + (size_t)rows * Hd;
+    float* al = o + (size_t)rows * Hd;
+    float* be = al + (size_t)rows * H;
+    const float* cur = h_in;
+    const int64_t cu[2] = {0, rows};
+    gdn_problem p{};
+    p.num_seqs = 1;
+    p.num_heads = H;
+    p.d_k = p.d_v = d;
+    p.cu_seqlens = cu;
+    p.qkv_dtype = GDN_F32;
+    p.out_dtype = GDN_F32;
+    p.algo = GDN_ALGO_AUTO;
+    const size_t LW = group_layer_floats(g);
+    for (int l = 0; l < g->layers; ++l) {
+        const float* W = weights + (size_t)l * LW;
+        const float* Wq = W;
+        const float* Wk = Wq + (size_t)Hd * Dm;
+        const float* Wv = Wk + (size_t)Hd * Dm;
+        const float* wa = Wv + (size_t)Hd * Dm;
+        const float* wb = wa + (size_t)H * Dm;
+        const float* Wo = wb + (size_t)H * Dm;
+        const bool last = l + 1 == g->layers;
+        if (gdn::group::project(cur, rows, Dm, H, d, Wq, Wk, Wv, wa, wb, q, k, v, al, be, stream) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        // the end of the group needs only the state: the next group reads its own cached input
+        const gdn_status st = gdn_prefill_ckpt(&p, last ? nullptr : q, k, v, al, be, nullptr, last ? nullptr : o,
+                                               S_out + (size_t)l * H * d * d, nullptr, nullptr, nullptr, workspace,
+                                               ws_bytes, stream);
+        if (st != GDN_OK) return st;
+        if (!last) {
+            float* nxt = cur == hA ? hB : hA;
+            if (gdn::group::mix(cur, o, rows, Dm, Hd, Wo, nxt, stream) != cudaSuccess) return GDN_ERR_CUDA;
+            cur = nxt;
+        }
+    }
+    return GDN_OK;
+}
+
+}  // namespace
+
+GDN_EXPORT size_t gdn_group_scratch_bytes(const gdn_group* g, int64_t rows) {
+    if (!group_ok(g) || rows < 0) return 0;
+    return (size_t)rows * group_row_floats(g) * sizeof(float);
+}
+
+GDN_EXPORT gdn_status gdn_group_replay(const gdn_group* g, const float* h, int64_t m, int32_t r_num, int32_t r_den,
+                                       const float* weights, float* S_hat, float* S_exact, int64_t* a_out,
+                                       int64_t* k_out, void* scratch, size_t scratch_bytes, void* workspace,
+                                       size_t ws_bytes, gdn_stream_t stream) {
+    if (!group_ok(g)) return GDN_ERR_INVALID_ARG;
+    if (m < 0 || m >= ((int64_t)1 << 31) - 64 || !h || !weights || !S_hat || !aligned(S_hat, 16) || !aligned(h, 16) ||
+        !aligned(weights, 16))
+        return GDN_ERR_INVALID_ARG;
+    if (S_exact && !aligned(S_exact, 16)) return GDN_ERR_INVALID_ARG;
+    int64_t a = 0, kk = 0;
+    if (gdn_replay_plan(m, r_num, r_den, &a, &kk) != GDN_OK) return GDN_ERR_INVALID_ARG;
+    const int64_t rows = S_exact ? m : kk;
+    if (!scratch || !aligned(scratch, 16) || scratch_bytes < gdn_group_scratch_bytes(g, rows))
+        return GDN_ERR_INVALID_ARG;
+    gdn_status st;
+    if ((st = check_workspace(workspace, ws_bytes)) != GDN_OK) return st;
+    if (a_out) *a_out = a;
+    if (k_out) *k_out = kk;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (S_exact && (st = group_chain(g, h, m, weights, S_exact, static_cast<float*>(scratch), workspace, ws_bytes, s)) !=
+                       GDN_OK)
+        return st;
+    return group_chain(g, h + (size_t)a * g->d_model, kk, weights, S_hat, static_cast<float*>(scratch), workspace,
+                       ws_bytes, s);
 }

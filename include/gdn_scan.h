@@ -235,6 +235,48 @@ gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, co
                                     int32_t rmax_num, int32_t rmax_den, int64_t* k_out, int32_t* exact_out);
 
 /*
+ * In-group chained replay ("Tail-Replay" notes page, section 2.2 step 3 and
+ * section 2.4): the linear-attention layers of one group are replayed one after
+ * the other from zero states over the tail a+1..m (k = ceil(r m) exact, a = m - k),
+ * the first layer reading the group's exact cached input hidden states h and every
+ * later layer the previous layer's replayed outputs; the last layer needs only its
+ * state (its output feeds nothing the recovery uses).  With S_exact the same
+ * chain also runs over 1..m (the full prefill) for comparison.
+ *
+ * The pages fix no model, so the group is synthetic, with weights given per layer
+ * l (fp32, contiguous, layer after layer; D = d_model, Hd = heads * d_head):
+ *   W_q [Hd, D], W_k [Hd, D], W_v [Hd, D], w_a [heads, D], w_b [heads, D], W_o [D, Hd]
+ * and, per token t and head: q = W_q h / |W_q h|, k = W_k h / |W_k h|, v = W_v h,
+ * alpha = 1 - 0.1 sigmoid(w_a . h), beta = sigmoid(w_b . h); next layer's input
+ * h + W_o [o_1; ...; o_heads] (o_t = S_t q_t per head).
+ *
+ *  g          layers 1..64, heads 1..1024, d_model 1..8192, d_head in {32, 64, 128},
+ *             heads * d_head <= 8192
+ *  h          device [m, d_model] fp32 (one request's rows)
+ *  weights    device, layers * (4 Hd + 2 heads) * d_model floats
+ *  S_hat      device [layers, heads, d_head, d_head] fp32 out (replayed states at m)
+ *  S_exact    device, same shape, or null (skip the full chain)
+ *  a_out, k_out  host int64 out (nullable)
+ *  scratch    device, 16-byte aligned, at least gdn_group_scratch_bytes(g, rows)
+ *             bytes with rows = m when S_exact is given, else k
+ *  workspace  as for the other device entry points
+ * Invalid arguments: GDN_ERR_INVALID_ARG before anything is enqueued.
+ */
+typedef struct gdn_group {
+    int32_t layers;
+    int32_t heads;
+    int32_t d_model;
+    int32_t d_head;
+} gdn_group;
+
+size_t gdn_group_scratch_bytes(const gdn_group* g, int64_t rows);
+
+gdn_status gdn_group_replay(const gdn_group* g, const float* h, int64_t m, int32_t r_num, int32_t r_den,
+                            const float* weights, float* S_hat, float* S_exact, int64_t* a_out, int64_t* k_out,
+                            void* scratch, size_t scratch_bytes, void* workspace, size_t ws_bytes,
+                            gdn_stream_t stream);
+
+/*
  * Prefill with sparse checkpoints for callers that cannot allocate device memory.
  * (No counterpart on the pages: this is a calling convention of this library.)
  *

@@ -298,3 +298,25 @@ def depth_weights(kind: str, N: int, n_requests: int, seed: int = 0) -> List[int
         for i in range(n_requests):
             w[0 if coin[i] == 0 else (u1[i] + u2[i]) // 2] += 1
     return w
+
+
+# --------------------------------------------------------------------------------------------
+# synthetic linear-attention group for chained replay (its weights are inputs of the method)
+# --------------------------------------------------------------------------------------------
+def group_weights(seed: int, layers: int, heads: int, d_model: int, d_head: int, device="cpu") -> torch.Tensor:
+    """Flat fp32 weights, layer after layer: W_q, W_k, W_v [heads d_head, d_model] and w_a, w_b
+    [heads, d_model] with N(0, 1/d_model) entries, W_o [d_model, heads d_head] with N(0, 1/(4 heads d_head))."""
+    Hd = heads * d_head
+    parts = []
+    for l in range(layers):
+        base = 300 + 8 * l
+        for j, (n, sc) in enumerate(((Hd * d_model, d_model ** -0.5), (Hd * d_model, d_model ** -0.5),
+                                     (Hd * d_model, d_model ** -0.5), (heads * d_model, d_model ** -0.5),
+                                     (heads * d_model, d_model ** -0.5), (d_model * Hd, 0.5 * Hd ** -0.5))):
+            parts.append(normal(seed, base + j, 0, (n,), sc, device=device))
+    return torch.cat(parts)
+
+
+def group_inputs(seed: int, rows: int, d_model: int, device="cpu") -> torch.Tensor:
+    """The group's cached input hidden states h [rows, d_model], N(0, 1) fp32."""
+    return normal(seed, 299, 0, (rows, d_model), 1.0, device=device)

@@ -143,3 +143,25 @@ def test_overlap_gives_identical_states_and_hides_the_shorter_leg():
     assert shorter > 0.3 * longer, "the two legs should be comparable for this check"
     assert t_ovl < t_ser - 0.5 * shorter, "the overlap hides less than half of the shorter leg"
     assert t_ovl > 0.9 * longer, "faster than the longer leg alone: the timing is not what it seems"
+
+
+@pytest.mark.parametrize("L,H,Dm,d,m,rn,rd", [(3, 4, 256, 64, 700, 1, 10), (2, 2, 128, 128, 300, 1, 20),
+                                              (2, 3, 96, 32, 129, 1, 1)])
+def test_group_replay_matches_oracle(L, H, Dm, d, m, rn, rd):
+    from oracle import group as G
+    w = synth.group_weights(7, L, H, Dm, d)
+    h = synth.group_inputs(7, m, Dm)
+    r = gdn.gdn_group_replay(h.to(DEV), w.to(DEV), L, H, Dm, d, m, rn, rd)
+    torch.cuda.synchronize()
+    ref = G.group_replay(h, w, L, H, Dm, d, m, rn, rd)
+    assert (r["a"], r["k"]) == (ref["a"], ref["k"])
+    errs = []
+    for l in range(L):
+        for hh in range(H):
+            assert_close(r["S_hat"][l, hh], ref["S_hat"][l][hh], f"group S_hat layer {l} head {hh}")
+            assert_close(r["S_exact"][l, hh], ref["S_exact"][l][hh], f"group S_exact layer {l} head {hh}")
+            e = np.linalg.norm(ref["S_exact"][l][hh] - ref["S_hat"][l][hh]) / np.linalg.norm(ref["S_exact"][l][hh])
+            errs.append(round(float(e), 4))
+    print(f"relative replay error per (layer, head): {errs}")
+    if rn == rd:
+        assert torch.equal(r["S_hat"], r["S_exact"])
