@@ -220,9 +220,10 @@ __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) 
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(x - __uint_as_float(hi)));
 }
 // d (16 x 8, m16n8 accumulator layout) += A (16 x 8, row-major at a, row stride lda) B (8 x 8, row-major
-// at b, row stride ldb), as hi*hi + hi*lo + lo*hi with mma.sync m16n8k8 tf32 (fp32 accumulate)
-__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const float* a, int lda, const float* b, int ldb, int g8,
-                                           int t4) {
+// at b, row stride ldb) as hi*hi, and c += hi*lo + lo*hi (mma.sync m16n8k8 tf32, fp32 accumulate); two
+// accumulators keep the dependent MMA chains short; the caller adds c to d at the end
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], float (&c)[4], const float* a, int lda, const float* b,
+                                           int ldb, int g8, int t4) {
     uint32_t ah[4], al[4], bh[2], bl[2];
     tf32_split(a[g8 * lda + t4], ah[0], al[0]);
     tf32_split(a[(g8 + 8) * lda + t4], ah[1], al[1]);
@@ -230,14 +231,14 @@ __device__ __forceinline__ void mma_tf32x3(float (&d)[4], const float* a, int ld
     tf32_split(a[(g8 + 8) * lda + t4 + 4], ah[3], al[3]);
     tf32_split(b[t4 * ldb + g8], bh[0], bl[0]);
     tf32_split(b[(t4 + 4) * ldb + g8], bh[1], bl[1]);
-#define GDN_MMA_TF32(A, B)                                                                                      \
+#define GDN_MMA_TF32(D, A, B)                                                                                   \
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, " \
                  "{%0,%1,%2,%3};"                                                                               \
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])                                              \
+                 : "+f"(D[0]), "+f"(D[1]), "+f"(D[2]), "+f"(D[3])                                              \
                  : "r"(A[0]), "r"(A[1]), "r"(A[2]), "r"(A[3]), "r"(B[0]), "r"(B[1]))
-    GDN_MMA_TF32(al, bh);
-    GDN_MMA_TF32(ah, bl);
-    GDN_MMA_TF32(ah, bh);
+    GDN_MMA_TF32(c, al, bh);
+    GDN_MMA_TF32(d, ah, bh);
+    GDN_MMA_TF32(c, ah, bl);
 #undef GDN_MMA_TF32
 }
 __device__ __forceinline__ void group_sync(int id, int n) {
@@ -307,13 +308,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     // TMA and MMA completions (one arrival each)
     uint64_t* bar_kq = bars + 0;       // [2] K/Q tiles landed
     uint64_t* bar_v = bars + 2;        // V tile landed
-    uint64_t* bar_g = bars + 3;        // [K; Q] K^T done (its Q rows give P)
+    uint64_t* bar_g = bars + 3;        // [K; Q] K^T done (its K rows give L, its Q rows P)
     uint64_t* bar_wu = bars + 4;       // W^T, U~^T done
     uint64_t* bar_uo = bars + 5;       // U^T done
     uint64_t* bar_st = bars + 6;       // state update and every MMA issued before it done
     uint64_t* bar_o = bars + 7;        // St Q^T + U''^T P^T done
     // operands ready for the issuing warp, or results read
-    uint64_t* bar_gin = bars + 8;      // prep: K/Q/V tiles padded, G columns free           (1 arrival)
+    uint64_t* bar_gin = bars + 8;      // prep: K/Q tiles padded, G columns free             (1 arrival)
     uint64_t* bar_wuin = bars + 9;     // prep: T diag(.) operands in shared memory           (1)
     uint64_t* bar_wready = bars + 10;  // prep: -sigma_0 W in shared memory                   (NPREP)
     uint64_t* bar_pready = bars + 11;  // prep: P in shared memory                            (NPREP)
@@ -706,76 +707,74 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         proxy_fence();
         group_sync(BAR_PREP, NPREP);
 
-        for (int j = 0;; ++j) {
+        // chunk jj's K/Q landed and its rows past the chunk zeroed; then [K; Q] K^T can be issued
+        auto stage_kq = [&](int jj) -> bool {
+            if (!group_wait(&bar_kq[jj & 1], (uint32_t)((jj >> 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
+                return false;
+            const int nn = ring[jj % kRing].n;
+            if (nn < C) {
+                const int nz = C - nn;
+                for (int i = ptid; i < 4 * nz * 8; i += NPREP) {
+                    const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;   // K / Q x two column blocks
+                    unsigned char* base = smem + OFF_KQ + (jj & 1) * 32768 + (part >> 1) * 16384 + (part & 1) * 8192;
+                    *reinterpret_cast<uint4*>(base + (nn + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                proxy_fence();
+            }
+            tc_fence_before();   // the G columns were last read by the previous chunk's P extraction
+            group_sync(BAR_PREP, NPREP);
+            if (leader) mbar_arrive(bar_gin);
+            return true;
+        };
+        bool staged = stage_kq(0);
+
+        for (int j = 0; staged; ++j) {
             const Ring& R = ring[j % kRing];
             const int n = R.n;
             const bool single = R.single != 0;
             const bool last = R.last != 0;
             const float* ps = psc + (j & 1) * 4 * C;
 
-            // ---- this chunk's K, Q, V; zero the tile rows past the chunk ----
-            if (!group_wait(&bar_kq[j & 1], (uint32_t)((j >> 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit) ||
-                !group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
-                break;
+            // ---- this chunk's V (rows past the chunk zeroed); its [K; Q] K^T was issued a chunk ago ----
+            if (!group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             if (n < C) {
                 const int nz = C - n;
-                for (int i = ptid; i < 6 * nz * 8; i += NPREP) {
-                    const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;   // part 0-3: [K;Q], 4-5: V
-                    unsigned char* base = part < 4 ? smem + OFF_KQ + (j & 1) * 32768 + (part >> 1) * 16384 + (part & 1) * 8192
-                                                   : smem + OFF_V + (part - 4) * 8192;
-                    *reinterpret_cast<uint4*>(base + (n + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = ptid; i < 2 * nz * 8; i += NPREP) {
+                    const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;
+                    *reinterpret_cast<uint4*>(smem + OFF_V + part * 8192 + (n + rz) * 128 + seg * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
                 proxy_fence();
             }
-            tc_fence_before();
-            group_sync(BAR_PREP, NPREP);
-            if (leader) mbar_arrive(bar_gin);   // [K; Q] K^T on tcgen05, for P at the end of this iteration
-
-            // ---- K K^T on mma.sync (exact bf16 inputs) for L: warp = (row tile mt, column half); column tiles
-            //      wholly above the diagonal are zero in L and skipped ----
+            if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+            tc_fence_after();
             const int g8 = lane >> 2, t4 = lane & 3;
-            {
-                const uint32_t inKQ = sbase + OFF_KQ + (j & 1) * 32768;
-                const int mt = pw >> 1, nb = 32 * (pw & 1);
-                const int njp = (nb >= 16 * (mt + 1)) ? 0 : (nb + 16 >= 16 * (mt + 1) ? 1 : 2);   // live column pairs
-                float ga[4][4];
+            // ---- L (fp32, zero on and above the diagonal) from the K rows of [K; Q] K^T; diagonal blocks to Ld ----
+            if (lq < 2) {
+                const int t = row, s0 = 32 * half;
+                float gi[32];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) ga[jj][e] = 0.f;
-                if (njp > 0) {
-#pragma unroll
-                    for (int kt = 0; kt < 8; ++kt) {
-                        uint32_t ak[4];
-                        ldsm4(inKQ + kq_off(16 * mt + (lane & 15), 16 * kt + 8 * (lane >> 4)), ak);
-#pragma unroll
-                        for (int jp = 0; jp < 2; ++jp) {
-                            if (jp < njp) {
-                                uint32_t b[4];
-                                ldsm4(inKQ + kq_off(nb + 16 * jp + 8 * (lane >> 4) + (lane & 7), 16 * kt + 8 * ((lane >> 3) & 1)),
-                                      b);
-                                mma_bf16(ga[2 * jp], ak, b[0], b[1]);
-                                mma_bf16(ga[2 * jp + 1], ak, b[2], b[3]);
-                            }
-                        }
-                    }
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(ps + C + s0 + i);
+                    gi[i] = x.x;
+                    gi[i + 1] = x.y;
+                    gi[i + 2] = x.z;
+                    gi[i + 3] = x.w;
                 }
-                // L[t][s] = beta_t gamma_t / gamma_s (k_t . k_s) for s < t, else 0; diagonal 16-blocks also to Ld
+                const float f = ps[2 * C + t];
+                float v[32];
+                tmem_ld32(trow + T_G + 32 * half, v);
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
+                for (int i = 0; i < 32; ++i) v[i] = (s0 + i < t) ? f * gi[i] * v[i] : 0.f;
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int t = 16 * mt + g8 + 8 * hh, s2 = nb + 8 * jj + 2 * t4;
-                        const float f = ps[2 * C + t];
-                        const float l0 = s2 < t ? f * ps[C + s2] * ga[jj][2 * hh] : 0.f;
-                        const float l1 = s2 + 1 < t ? f * ps[C + s2 + 1] * ga[jj][2 * hh + 1] : 0.f;
-                        *reinterpret_cast<float2*>(Lf + t * kLdF + s2) = make_float2(l0, l1);
-                        if ((s2 >> 4) == (t >> 4)) {
-                            float* dd = Ld + (t >> 4) * 16 * 17 + (t & 15) * 17 + (s2 & 15);
-                            dd[0] = l0;
-                            dd[1] = l1;
-                        }
-                    }
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<float4*>(Lf + t * kLdF + s0 + 4 * q4) =
+                        make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                if ((t >> 5) == half) {   // the diagonal 16-block of row t lies in this half
+                    float* dst = Ld + (t >> 4) * 16 * 17 + (t & 15) * 17;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dst[i] = (lane & 16) ? v[16 + i] : v[i];
+                }
             }
             group_sync(BAR_PREP, NPREP);
             const float* sg_bg = ps + 2 * C;
@@ -821,12 +820,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         const int jb = 2 * qw, ib = jb + 1;
                         float* sc = Ld + jb * 16 * 17;   // this warp's diagonal blocks are no longer needed
                         float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        float yc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                             for (int ks = 0; ks < 2; ++ks)
-                                mma_tf32x3(y[nt], Lf + (16 * ib) * kLdF + 16 * jb + 8 * ks, kLdF,
+                                mma_tf32x3(y[nt], yc[nt], Lf + (16 * ib) * kLdF + 16 * jb + 8 * ks, kLdF,
                                            Lf + (16 * jb + 8 * ks) * kLdF + 16 * jb + 8 * nt, kLdF, g8, t4);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) y[nt][e] += yc[nt][e];
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             sc[g8 * 16 + 8 * nt + 2 * t4] = y[nt][0];
@@ -836,12 +840,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         }
                         __syncwarp();
                         float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        float xc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                             for (int ks = 0; ks < 2; ++ks)
-                                mma_tf32x3(x[nt], Lf + (16 * ib) * kLdF + 16 * ib + 8 * ks, kLdF, sc + 8 * ks * 16 + 8 * nt,
-                                           16, g8, t4);
+                                mma_tf32x3(x[nt], xc[nt], Lf + (16 * ib) * kLdF + 16 * ib + 8 * ks, kLdF,
+                                           sc + 8 * ks * 16 + 8 * nt, 16, g8, t4);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) x[nt][e] += xc[nt][e];
                         float* dst = Lf + (16 * ib) * kLdF + 16 * jb;
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
@@ -883,22 +892,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             group_sync(BAR_PREP, NPREP);
             {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block on mma.sync tf32; warp = (row, column) tile
                 const int mt = pw >> 2, nt = pw & 3;
-                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                float y[4] = {0.f, 0.f, 0.f, 0.f}, yc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32x3(y, Lf + (32 + 16 * mt) * kLdF + 8 * ks, kLdF, Lf + (8 * ks) * kLdF + 8 * nt, kLdF,
+                    mma_tf32x3(y, yc, Lf + (32 + 16 * mt) * kLdF + 8 * ks, kLdF, Lf + (8 * ks) * kLdF + 8 * nt, kLdF,
                                g8, t4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] += yc[e];
                 // L_BA T_AA as [32][33] scratch
                 Yb[(16 * mt + g8) * 33 + 8 * nt + 2 * t4] = y[0];
                 Yb[(16 * mt + g8) * 33 + 8 * nt + 2 * t4 + 1] = y[1];
                 Yb[(16 * mt + g8 + 8) * 33 + 8 * nt + 2 * t4] = y[2];
                 Yb[(16 * mt + g8 + 8) * 33 + 8 * nt + 2 * t4 + 1] = y[3];
                 group_sync(BAR_PREP, NPREP);
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                float x[4] = {0.f, 0.f, 0.f, 0.f}, xc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32x3(x, Lf + (32 + 16 * mt) * kLdF + 32 + 8 * ks, kLdF, Yb + (8 * ks) * 33 + 8 * nt, 33,
+                    mma_tf32x3(x, xc, Lf + (32 + 16 * mt) * kLdF + 32 + 8 * ks, kLdF, Yb + (8 * ks) * 33 + 8 * nt, 33,
                                g8, t4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[e] += xc[e];
                 put_t12(32 + 16 * mt + g8, 8 * nt + 2 * t4, -x[0], -x[1]);
                 put_t12(32 + 16 * mt + g8 + 8, 8 * nt + 2 * t4, -x[2], -x[3]);
             }
@@ -906,6 +919,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             group_sync(BAR_PREP, NPREP);
             if (leader) mbar_arrive(bar_wuin);
 
+            // ---- while W^T and U~^T are computed: P = mask(q_t . k_s) from the Q rows of [K; Q] K^T, once the
+            //      chain's previous U''^T P^T is done ----
+            if (rd) {
+                if (j > 0 && !group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
+                    break;
+                tc_fence_after();
+                if (lq >= 2) {
+                    float v[32];
+                    tmem_ld32(trow + T_G + 32 * half, v);
+                    const int t = row - 64, s0 = 32 * half;
+                    if (single && t == 0 && half == 0) ring[j % kRing].qk0 = v[0];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = (!single && s0 + i <= t) ? v[i] : 0.f;
+                    st_split32(smem + OFF_PH, smem + OFF_PL, t, s0, v);
+                }
+                proxy_fence();
+                tc_fence_before();
+                mbar_arrive(bar_pready);
+            }
+            // ---- the next chunk's [K; Q] K^T, now that the G columns are free: it runs beside this chunk's
+            //      W and U~ and is ready when the next iteration starts ----
+            if (!last && !(staged = stage_kq(j + 1))) break;
             // ---- W^T = K^T T1^T, U~^T = V^T T2^T; then -sigma_0 W^T as the MN-major B operand ----
             if (!group_wait(bar_wu, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             tc_fence_after();
@@ -922,25 +957,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             tc_fence_before();
             mbar_arrive(bar_wready);
 
-            // ---- P = mask(q_t . k_s) from the Q rows of [K; Q] K^T, once the chain's previous U''^T P^T is done ----
-            if (rd) {
-                if (j > 0 && !group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
-                    break;
-                if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
-                tc_fence_after();
-                if (lq >= 2) {
-                    float v[32];
-                    tmem_ld32(trow + T_G + 32 * half, v);
-                    const int t = row - 64, s0 = 32 * half;
-                    if (single && t == 0 && half == 0) ring[j % kRing].qk0 = v[0];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = (!single && s0 + i <= t) ? v[i] : 0.f;
-                    st_split32(smem + OFF_PH, smem + OFF_PL, t, s0, v);
-                }
-                proxy_fence();
-                tc_fence_before();
-                mbar_arrive(bar_pready);
-            }
             if (last) break;
         }
     } else if (lane == 0) {
@@ -958,16 +974,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
                 if (sp == 0 && mbar_test(bar_gin, jp & 1)) {
                     tc_fence_after();
-                    if (rd) {
-                        // [K; Q] K^T (its Q rows give P)
+                    // [K; Q] K^T: its K rows give L, its Q rows P
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
-                        }
-                        umma_commit(bar_g);
-                        ++cnt[2];
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
                     }
+                    umma_commit(bar_g);
+                    ++cnt[2];
                     sp = 1;
                     progressed = true;
                 }
