@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn_scan.so")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_TIMEOUT = range(5)
 GDN_F32, GDN_BF16 = 0, 1
-ALGO = {"auto": 0, "per_token": 1, "chunked": 2, "chunked_mma": 3}
+ALGO = {"auto": 0, "per_token": 1, "chunked": 2, "chunked_mma": 3, "two_pass": 4}
 PLACE = {"dp": 0, "balanced": 1, "block": 2, "random": 3, "greedy": 4}
 
 _lock = threading.Lock()
@@ -89,6 +89,8 @@ def lib():
             L.gdn_expected_recompute.argtypes = [pi64, i64, pi64, i32, pi64]
             L.gdn_workspace_size.argtypes = []
             L.gdn_workspace_size.restype = sz
+            L.gdn_workspace_size_two_pass.argtypes = [i64, i32, i32]
+            L.gdn_workspace_size_two_pass.restype = sz
             L.gdn_clear_status.argtypes = [vp, sz, vp]
             L.gdn_read_status.argtypes = [vp, sz, vp]
             L.gdn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -141,15 +143,29 @@ def _dtype_code(dt: torch.dtype) -> int:
     raise ValueError(f"unsupported dtype {dt}")
 
 
-def workspace(device) -> torch.Tensor:
-    """The cached per-device workspace (holds the sticky device status word)."""
+def workspace(device, nbytes: int = 0) -> torch.Tensor:
+    """The cached per-device workspace (holds the sticky device status word), grown to at least
+    `nbytes`; growing keeps the status word."""
     device = torch.device(device)
     idx = device.index if device.index is not None else torch.cuda.current_device()
     ws = _workspaces.get(idx)
-    if ws is None:
-        ws = torch.zeros(int(lib().gdn_workspace_size()), dtype=torch.uint8, device=torch.device("cuda", idx))
+    need = max(int(lib().gdn_workspace_size()), int(nbytes))
+    if ws is None or ws.numel() < need:
+        new = torch.zeros(need, dtype=torch.uint8, device=torch.device("cuda", idx))
+        if ws is not None:
+            new[:int(lib().gdn_workspace_size())].copy_(ws[:int(lib().gdn_workspace_size())])
+        ws = new
         _workspaces[idx] = ws
     return ws
+
+
+def _auto_ws(dev, algo: str, k, v, tokens: int, ranges: int) -> torch.Tensor:
+    """The cached workspace, large enough for the two-pass chunked path when the call may take it."""
+    H, dk, dv = k.shape[1], k.shape[2], v.shape[-1]
+    nbytes = 0
+    if algo in ("auto", "two_pass") and dk == 128 and dv == 128 and k.dtype == torch.bfloat16 and tokens > 0:
+        nbytes = int(lib().gdn_workspace_size_two_pass(int(tokens), int(H), int(ranges)))
+    return workspace(dev, nbytes)
 
 
 def read_status(device=None, stream=None, ws: Optional[torch.Tensor] = None) -> int:
@@ -264,7 +280,7 @@ def gdn_prefill_ckpt(q, k, v, alpha, beta, cu_seqlens, *, S0=None, ckpt_pos=None
     n_ck = 0 if cu_ck is None else int(cu_ck[-1])
     if ckpt_states is None and n_ck > 0:
         ckpt_states = torch.empty((n_ck, H, dv, dk), dtype=torch.float32, device=dev)
-    ws = ws if ws is not None else workspace(dev)
+    ws = ws if ws is not None else _auto_ws(dev, algo, k, v, T, B)
     pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_prefill_ckpt(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
                                 _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
@@ -305,7 +321,7 @@ def gdn_resume_from_ckpt(q, k, v, alpha, beta, cu_seqlens, ckpt_states, ckpt_pos
         o_out = None
     if S_out is None:
         S_out = torch.empty((P, H, dv, dk), dtype=torch.float32, device=dev)
-    ws = ws if ws is not None else workspace(dev)
+    ws = ws if ws is not None else _auto_ws(dev, algo, k, v, int(deps.sum()) if P else 0, P)
     pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_resume_from_ckpt(
         ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0),
@@ -340,7 +356,8 @@ def gdn_tail_replay(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int,
         o = None
     a_out = np.zeros(B, dtype=np.int64)
     k_out = np.zeros(B, dtype=np.int64)
-    ws = ws if ws is not None else workspace(dev)
+    twin = 2 if S_a is not None else 1
+    ws = ws if ws is not None else _auto_ws(dev, algo, k, v, int(mm.sum()) * twin, B * twin)
     pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_tail_replay(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
                                _ptr(beta), _p64(mm), r_num, r_den, _ptr(S_a), _ptr(S_hat),
@@ -377,10 +394,12 @@ def gdn_tail_replay_k(q, k, v, alpha, beta, cu_seqlens, m, k_replay, *, S_a=None
     B = len(cu) - 1
     T, H, dk, dv, dev, out_dtype, S_hat, S_exact, o = _replay_buffers(k, v, B, S_a, readout, out_dtype, S_hat,
                                                                       S_exact, o)
-    ws = ws if ws is not None else workspace(dev)
+    mm, kr = _i64(m), _i64(k_replay)
+    ws = ws if ws is not None else _auto_ws(dev, algo, k, v, int(kr.sum()) + (int(mm.sum()) if S_a is not None else 0),
+                                            B * (2 if S_a is not None else 1))
     pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_tail_replay_k(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha),
-                                 _ptr(beta), _p64(_i64(m)), _p64(_i64(k_replay)), _ptr(S_a), _ptr(S_hat),
+                                 _ptr(beta), _p64(mm), _p64(kr), _ptr(S_a), _ptr(S_hat),
                                  _ptr(S_exact if S_a is not None else None), _ptr(o), _ptr(ws), ws.numel(),
                                  _stream(stream, dev))
     _check(rc, "gdn_tail_replay_k")
@@ -402,10 +421,12 @@ def gdn_tail_replay_overlap(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_d
         raise ValueError("kv_host and kv_dev sizes differ")
     a_out = np.zeros(B, dtype=np.int64)
     k_out = np.zeros(B, dtype=np.int64)
-    ws = ws if ws is not None else workspace(dev)
+    mm = _i64(m)
+    twin = 2 if S_a is not None else 1
+    ws = ws if ws is not None else _auto_ws(dev, algo, k, v, int(mm.sum()) * twin, B * twin)
     pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
     rc = lib().gdn_tail_replay_overlap(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v),
-                                       _ptr(alpha), _ptr(beta), _p64(_i64(m)), r_num, r_den, _ptr(S_a), _ptr(S_hat),
+                                       _ptr(alpha), _ptr(beta), _p64(mm), r_num, r_den, _ptr(S_a), _ptr(S_hat),
                                        _ptr(S_exact if S_a is not None else None), _ptr(o), _p64(a_out),
                                        _p64(k_out), ctypes.c_void_p(kv_host.data_ptr()),
                                        ctypes.c_void_p(kv_dev.data_ptr()), nbytes, _ptr(ws), ws.numel(),

@@ -10,7 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", "gdn_scan")
 LIB = os.path.join(PKG, "libgdn_scan.so")
-SOURCES = ["gdn_api.cu", "gdn_noalloc.cu", "gdn_placement.cpp", "gdn_group.cu", "inst_chunk_tc.cu", "inst_dk32.cu", "inst_dk64.cu", "inst_dk128.cu"]
+SOURCES = ["gdn_api.cu", "gdn_noalloc.cu", "gdn_placement.cpp", "gdn_group.cu", "gdn_tprep.cu", "inst_chunk_tc.cu",
+           "inst_chunk_tc_pre.cu", "inst_dk32.cu", "inst_dk64.cu", "inst_dk128.cu"]
 HEADERS = [os.path.join(CSRC, f) for f in ("gdn_kernel.cuh", "gdn_chunk.cuh", "gdn_chunk_tc.cuh", "gdn_group.cuh")] + [
     os.path.join(ROOT, "include", "gdn_scan.h")]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

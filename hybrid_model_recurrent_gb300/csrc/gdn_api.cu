@@ -79,10 +79,12 @@ gdn_status check_problem(const gdn_problem* p, std::vector<int64_t>& lens) {
     if ((p->qkv_dtype != GDN_F32 && p->qkv_dtype != GDN_BF16) || (p->out_dtype != GDN_F32 && p->out_dtype != GDN_BF16))
         return GDN_ERR_INVALID_ARG;
     if (p->algo != GDN_ALGO_AUTO && p->algo != GDN_ALGO_PER_TOKEN && p->algo != GDN_ALGO_CHUNKED &&
-        p->algo != GDN_ALGO_CHUNKED_MMA)
+        p->algo != GDN_ALGO_CHUNKED_MMA && p->algo != GDN_ALGO_CHUNKED_TWO_PASS)
         return GDN_ERR_INVALID_ARG;
     if (!supported_d(p->d_k) || !supported_d(p->d_v)) return GDN_ERR_UNSUPPORTED;
-    if ((p->algo == GDN_ALGO_CHUNKED || p->algo == GDN_ALGO_CHUNKED_MMA) && !chunked_ok(p)) return GDN_ERR_UNSUPPORTED;
+    if ((p->algo == GDN_ALGO_CHUNKED || p->algo == GDN_ALGO_CHUNKED_MMA || p->algo == GDN_ALGO_CHUNKED_TWO_PASS) &&
+        !chunked_ok(p))
+        return GDN_ERR_UNSUPPORTED;
     if (p->cu_seqlens[0] != 0) return GDN_ERR_INVALID_ARG;
     lens.resize(p->num_seqs);
     for (int b = 0; b < p->num_seqs; ++b) {
@@ -112,6 +114,22 @@ gdn_status check_workspace(void* ws, size_t bytes) {
     return GDN_OK;
 }
 
+// Workspace of the two-pass chunked path: after the status word, the chunk counts [streams], the chunk
+// starts [rows] and T [rows][64] fp32, where rows = sum over the call's ranges of len x H.
+struct TwoPassLayout {
+    size_t cnt_off, beg_off, t_off, total;
+};
+constexpr int64_t kMaxTwoPassRows = ((int64_t)1 << 31) - 1;
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+TwoPassLayout two_pass_layout(int64_t rows, int64_t streams) {
+    TwoPassLayout l;
+    l.cnt_off = kWorkspaceBytes;
+    l.beg_off = round_up(l.cnt_off + 4 * (size_t)streams, 256);
+    l.t_off = round_up(l.beg_off + 4 * (size_t)rows, 256);
+    l.total = l.t_off + (size_t)rows * gdn::tc::C * sizeof(float);
+    return l;
+}
+
 // Validate one sequence's checkpoint list: strictly increasing in [1, n].
 bool ckpts_valid(const int64_t* c, int64_t M, int64_t n) {
     for (int64_t i = 0; i < M; ++i) {
@@ -138,7 +156,30 @@ struct LaunchSpec {
     unsigned int* status;
     bool readout;
     bool twin;
+    size_t ws_bytes;   // bytes at status (the caller's workspace)
 };
+
+// rows and streams of the two-pass path for a job list (the exact twins counted when `twin`)
+void two_pass_extent(const LaunchSpec& L, const std::vector<HostJob>& jobs, int64_t& rows, int64_t& streams) {
+    const int64_t H = L.p->num_heads, f = L.twin ? 2 : 1;
+    rows = 0;
+    for (const HostJob& j : jobs) rows += (int64_t)j.job.len * H * f;
+    streams = (int64_t)jobs.size() * H * f;
+}
+// the T kernel's grid has a block row per (job, head) of a launch: at most 65535
+bool two_pass_supported(const LaunchSpec& L) { return (int64_t)L.p->num_heads * gdn::kMaxJobs <= 65535; }
+bool two_pass_fits(const LaunchSpec& L, const std::vector<HostJob>& jobs) {
+    int64_t rows, streams;
+    two_pass_extent(L, jobs, rows, streams);
+    if (!two_pass_supported(L) || rows > kMaxTwoPassRows) return false;
+    return L.ws_bytes >= two_pass_layout(rows, streams).total;
+}
+// GDN_ALGO_CHUNKED_TWO_PASS with too small a workspace is an invalid argument, found before anything is enqueued
+gdn_status check_two_pass(const LaunchSpec& L, const std::vector<HostJob>& jobs) {
+    if (L.p->algo != GDN_ALGO_CHUNKED_TWO_PASS) return GDN_OK;
+    if (!two_pass_supported(L)) return GDN_ERR_UNSUPPORTED;
+    return two_pass_fits(L, jobs) ? GDN_OK : GDN_ERR_INVALID_ARG;
+}
 
 // Batch jobs into parameter blocks and launch each with `launch(params, n_jobs)`.
 template <class F>
@@ -187,6 +228,37 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
     auto prm = std::make_unique<gdn::Params>();
     std::memset(prm.get(), 0, sizeof(gdn::Params));
     const int D = gdn::chunk::D, C = gdn::chunk::C;
+    // two passes when asked for, or by default when the workspace holds T of every chunk
+    const bool warp_mma = p->algo == GDN_ALGO_CHUNKED_MMA;
+    bool two_pass = false;
+    if (p->algo == GDN_ALGO_CHUNKED_TWO_PASS || p->algo == GDN_ALGO_AUTO) {
+        LaunchSpec whole = L;
+        whole.twin = false;   // the twins are in `jobs` now
+        two_pass = two_pass_fits(whole, jobs);
+        if (p->algo == GDN_ALGO_CHUNKED_TWO_PASS && !two_pass) return GDN_ERR_INVALID_ARG;
+    }
+    if (two_pass) {
+        int64_t rows = 0;
+        for (HostJob& j : jobs) {
+            j.job.t_row0 = (int32_t)rows;
+            rows += (int64_t)j.job.len * H;
+        }
+        const TwoPassLayout lay = two_pass_layout(rows, (int64_t)jobs.size() * H);
+        unsigned char* ws = reinterpret_cast<unsigned char*>(L.status);
+        prm->chunk_cnt = reinterpret_cast<int32_t*>(ws + lay.cnt_off);
+        prm->chunk_beg = reinterpret_cast<int32_t*>(ws + lay.beg_off);
+        prm->t_rows = reinterpret_cast<float*>(ws + lay.t_off);
+        EncodeTiledFn enc = encode_fn();
+        if (!enc) return GDN_ERR_CUDA;
+        cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)std::max<int64_t>(rows, 1)};
+        cuuint64_t strides[1] = {(cuuint64_t)(C * sizeof(float))};
+        cuuint32_t box[2] = {(cuuint32_t)C, (cuuint32_t)C};
+        cuuint32_t estr[2] = {1u, 1u};
+        if (enc(&prm->tm_t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, prm->t_rows, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return GDN_ERR_CUDA;
+    }
     bool maps = true;
     if (L.k) maps = maps && make_stream_map(&prm->tm_k, L.k, true, T, H, D, 64, C, true);
     if (L.q) maps = maps && make_stream_map(&prm->tm_q, L.q, true, T, H, D, 64, C, true);
@@ -197,6 +269,7 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
     prm->alpha = L.alpha;
     prm->beta = L.beta;
     prm->o = L.o;
+    prm->o_vec16 = (L.o && aligned(L.o, 16)) ? 1 : 0;
     prm->ckpt_states = L.ckpt_states;
     prm->status = L.status;
     prm->wait_limit_ns = g_wait_ns.load();
@@ -204,10 +277,15 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
     prm->H = H;
     prm->dv = D;
     const bool out_bf16 = p->out_dtype == GDN_BF16;
-    const bool warp_mma = p->algo == GDN_ALGO_CHUNKED_MMA;
     return launch_batches(*prm, jobs, [&](const gdn::Params& pr, int nj) -> cudaError_t {
         const int grid = nj * H;
-        if (!warp_mma) return gdn::tc::launch(pr, grid, L.readout, out_bf16, stream);
+        if (two_pass) {
+            cudaError_t e = gdn::tc::launch_schedule(pr, grid, stream);
+            if (e == cudaSuccess) e = gdn::tc::launch_tprep(pr, grid, stream);
+            if (e == cudaSuccess) e = gdn::tc::launch(pr, grid, L.readout, out_bf16, true, stream);
+            return e;
+        }
+        if (!warp_mma) return gdn::tc::launch(pr, grid, L.readout, out_bf16, false, stream);
         if (L.readout)
             return out_bf16 ? gdn::chunk::launch_chunk<true, true>(pr, grid, stream)
                             : gdn::chunk::launch_chunk<false, true>(pr, grid, stream);
@@ -308,6 +386,12 @@ GDN_EXPORT gdn_status gdn_select_ckpt(const int64_t* c, int32_t M, int64_t d, in
 
 GDN_EXPORT size_t gdn_workspace_size(void) { return kWorkspaceBytes; }
 
+GDN_EXPORT size_t gdn_workspace_size_two_pass(int64_t tokens, int32_t num_heads, int32_t num_ranges) {
+    if (tokens < 0 || num_heads < 1 || num_ranges < 0) return 0;
+    if (tokens > kMaxTwoPassRows / num_heads) return 0;
+    return two_pass_layout(tokens * num_heads, (int64_t)num_ranges * num_heads).total;
+}
+
 GDN_EXPORT void gdn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
 
 GDN_EXPORT void gdn_debug_stall_after(int32_t chunks) { g_stall_after.store(chunks < 0 ? -1 : chunks); }
@@ -381,7 +465,9 @@ GDN_EXPORT gdn_status gdn_prefill_ckpt(const gdn_problem* p, const void* q, cons
             for (int64_t i = cu_ckpt[b]; i < cu_ckpt[b + 1]; ++i)
                 jobs[b].ckpts.push_back(gdn::Ckpt{(int32_t)ckpt_pos[i], (int32_t)i});
     }
-    LaunchSpec L{p, q, k, v, alpha, beta, o, ckpt_states, static_cast<unsigned int*>(workspace), o != nullptr, false};
+    LaunchSpec L{p, q, k, v, alpha, beta, o, ckpt_states, static_cast<unsigned int*>(workspace), o != nullptr, false,
+                 ws_bytes};
+    if ((st = check_two_pass(L, jobs)) != GDN_OK) return st;
     return run_jobs(L, jobs, (cudaStream_t)stream);
 }
 
@@ -439,11 +525,12 @@ GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, 
     }
     offs[num_probes] = total;
     if ((st = check_streams(p, q, k, v, alpha, beta, o_out != nullptr, total > 0)) != GDN_OK) return st;
+    LaunchSpec L{p, q, k, v, alpha, beta, o_out, nullptr, static_cast<unsigned int*>(workspace), o_out != nullptr,
+                 false, ws_bytes};
+    if ((st = check_two_pass(L, jobs)) != GDN_OK) return st;
     if (chosen_pos) std::copy(chosen.begin(), chosen.end(), chosen_pos);
     if (o_offsets) std::copy(offs.begin(), offs.end(), o_offsets);
     if (num_probes == 0) return GDN_OK;
-    LaunchSpec L{p, q, k, v, alpha, beta, o_out, nullptr, static_cast<unsigned int*>(workspace), o_out != nullptr,
-                 false};
     return run_jobs(L, jobs, (cudaStream_t)stream);
 }
 
@@ -484,8 +571,8 @@ static gdn_status replay_prepare(const gdn_problem* p, const void* q, const void
     }
     if ((st = check_streams(p, q, k, v, alpha, beta, o != nullptr, total > 0)) != GDN_OK) return st;
     L = LaunchSpec{p, q, k, v, alpha, beta, o, nullptr, static_cast<unsigned int*>(workspace), o != nullptr,
-                   S_a != nullptr};
-    return GDN_OK;
+                   S_a != nullptr, ws_bytes};
+    return check_two_pass(L, jobs);
 }
 
 static gdn_status replay_k(const gdn_problem* p, const void* q, const void* k, const void* v, const float* alpha,

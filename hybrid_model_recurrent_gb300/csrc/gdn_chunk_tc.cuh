@@ -38,10 +38,11 @@
 //       T diag(.) operands, -sigma_0 W, P, and (one warp) the gates and the chunk schedule one
 //       chunk further ahead;
 //   issue (warp 12, one lane) - every tcgen05.mma: the chain's U^T += St (-sigma_0 W)^T, St Q^T,
-//       St += U''^T K, U''^T P^T and the prep's [K; Q] K^T (for P), W^T, U~^T, each as soon as the
+//       St += U''^T K, U''^T P^T and the prep's [K; Q] K^T (L and P), W^T, U~^T, each as soon as the
 //       mbarriers of its operands have fired, so that no converting warp waits on a full MMA queue.
-// K K^T for L, on the prep stage's critical path, runs on mma.sync inside the prep warps (exact bf16
-// inputs), which turn its accumulators into L directly.
+// The prep warps stage the K/Q tiles of chunk j+1 as soon as they have read P_j out of the G
+// columns, so [K; Q] K^T of the next chunk runs beside W^T, U~^T of this one and L is waiting in
+// TMEM when the next iteration starts.
 // They hand over through mbarriers; each group agrees on every wait by a barrier reduction, so a
 // wait that runs out ends every loop without leaving a named barrier half-entered.
 //
@@ -98,7 +99,9 @@ constexpr int OFF_PSC = 218368;        // fp32 prep scalars [2][4][64]: gamma, 1
 constexpr int OFF_RING = 220416;       // Ring[kRing]
 constexpr int OFF_BAR = OFF_RING + kRing * 576;
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = OFF_BAR + kBarBytes + 1024;
+constexpr int OFF_OST = OFF_BAR + kBarBytes;   // 4 x 2 KB: readout staging, one [tokens][32 rows] tile per chain warp
+constexpr int kSmemBytes = OFF_OST + 4 * 2048 + 1024;
+static_assert(kSmemBytes <= 232448, "227 KB of shared memory per block");
 constexpr int kLdF = 68;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(OFF_PSC + 2 * 4 * C * 4 == OFF_RING, "scalar area");
@@ -197,23 +200,6 @@ __device__ __forceinline__ void st_split32(unsigned char* th, unsigned char* tl,
         *reinterpret_cast<uint4*>(tl + sw128(row, c0 + 8 * q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
 }
-// mma.sync m16n8k16 (row.col, bf16 -> f32) with operands from ldmatrix
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// byte offset of element (row, col) in the [K; Q] buffer (two 64-column blocks of [128 rows][128 B]); col % 8 == 0
-__device__ __forceinline__ uint32_t kq_off(int row, int col) {
-    return (uint32_t)((col >> 6) * 16384) + sw128(row, col & 63);
-}
 // x = hi + lo, both tf32 (10 explicit mantissa bits each)
 __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
@@ -240,6 +226,29 @@ __device__ __forceinline__ void mma_tf32x3(float (&d)[4], float (&c)[4], const f
     GDN_MMA_TF32(d, ah, bh);
     GDN_MMA_TF32(c, ah, bl);
 #undef GDN_MMA_TF32
+}
+// gamma over a window of up to 64 tokens held by one warp (token lane in a0, token 32 + lane in a1; 1 past
+// the window): inclusive products g0, g1 in token order, the same rounding wherever a chunk's gates are formed
+__device__ __forceinline__ void gate_prefix(float a0, float a1, float& g0, float& g1, int lane) {
+    g0 = a0;
+    g1 = a1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float x0 = __shfl_up_sync(0xffffffffu, g0, off);
+        const float x1 = __shfl_up_sync(0xffffffffu, g1, off);
+        if (lane >= off) {
+            g0 *= x0;
+            g1 *= x1;
+        }
+    }
+    g1 *= __shfl_sync(0xffffffffu, g0, 31);
+}
+// first token of the window whose gamma falls below 2^-32 (C if none); the chunk ends before it, or
+// after it when it is the first token
+__device__ __forceinline__ int gamma_first(float g0, float g1) {
+    const unsigned m0 = __ballot_sync(0xffffffffu, g0 < kGammaFloor);
+    const unsigned m1 = __ballot_sync(0xffffffffu, g1 < kGammaFloor);
+    return m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : C);
 }
 __device__ __forceinline__ void group_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -297,7 +306,7 @@ __device__ __forceinline__ void drain_phase(uint64_t* b, uint32_t parity, uint64
 // ------------------------------------------------------------------------------------
 // the kernel: one CTA = one (job, head)
 // ------------------------------------------------------------------------------------
-template <bool OUT_BF16, bool READOUT>
+template <bool OUT_BF16, bool READOUT, bool PRE_T>
 __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_constant__ Params p) {
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
     extern __shared__ unsigned char smem_raw[];
@@ -322,9 +331,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     uint64_t* bar_ofree = bars + 13;   // chain: O^T read out                                 (NCHAIN)
     uint64_t* bar_ufree = bars + 14;   // chain: U'' in shared memory, U^T columns free       (NCHAIN)
     uint64_t* bar_ring = bars + 15;    // [kRing] schedule entry written by the gate warp     (32)
+    uint64_t* bar_t = bars + 19;       // T tile of the chunk landed (T computed by the first passes)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 160);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 164);
-    int* cnt = reinterpret_cast<int*>(smem + OFF_BAR + 168);   // K/Q, V chunks issued; commits g, wu, uo, st, o
+    int* cnt = reinterpret_cast<int*>(smem + OFF_BAR + 168);   // K/Q, V chunks issued; commits g, wu, uo, st, o; T
     Ring* ring = reinterpret_cast<Ring*>(smem + OFF_RING);
     float* psc = reinterpret_cast<float*>(smem + OFF_PSC);
     float* Lf = reinterpret_cast<float*>(smem + OFF_LF);
@@ -360,8 +370,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         mbar_init(bar_ofree, NCHAIN);
         mbar_init(bar_ufree, NCHAIN);
         for (int i = 0; i < kRing; ++i) mbar_init(&bar_ring[i], 32);
+        mbar_init(bar_t, 1);
         *abort_flag = 0;
-        for (int i = 0; i < 7; ++i) cnt[i] = 0;
+        for (int i = 0; i < 8; ++i) cnt[i] = 0;
         fence_barrier_init();
     }
     tc_fence_before();
@@ -383,6 +394,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         tma_load_3d(dst + 16384 + 8192, &p.tm_q, 64, h, t0, &bar_kq[buf]);
         atomicMax(&cnt[0], c + 1);
     };
+    // T of chunk c (starting at token pos) from the rows the first passes wrote, into the L area
+    auto issue_t = [&](int c, int pos) {
+        proxy_fence();
+        mbar_arrive_expect_tx(bar_t, (uint32_t)(C * C * 4));
+        tma_load_2d(smem + OFF_LF, &p.tm_t, 0, job.t_row0 + h * len + pos, bar_t);
+        atomicMax(&cnt[7], c + 1);
+    };
     auto issue_v = [&](int c, int pos) {
         proxy_fence();
         mbar_arrive_expect_tx(bar_v, 2u * 8192u);
@@ -403,14 +421,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         }
     } else if (warp < 4) {
         // ============================ chain group ============================
-        auto split_state = [&](const Ring& R) {
-            // St -> bf16 hi/lo pairs (the A operand); a single small-alpha token then scales St
-            const bool single = R.single != 0;
-            const float f = R.prescale;
+        // St -> bf16 hi/lo pairs (the A operand of chunk Rn).  First, when the previous chunk Rp asks for it,
+        // sigma is folded into St and the folded state dumped (checkpoint); a single small-alpha token then
+        // scales St.  One pass over St: the fold costs no second read.
+        auto split_state = [&](const Ring& Rn, const Ring* Rp) {
+            const bool single = Rn.single != 0;
+            const float f = Rn.prescale;
+            const bool fold = Rp && Rp->fold != 0;
+            const float ff = fold ? Rp->sigma_after : 1.f;
+            float* d1 = (fold && Rp->dump_slot >= 0)
+                            ? p.ckpt_states + (size_t)Rp->dump_slot * (size_t)H * D * D + head_state
+                            : nullptr;
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 float v[32];
                 tmem_ld32(trow + T_S + 32 * cb, v);
+                if (fold) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= ff;
+                    if (!single) tmem_st32(trow + T_S + 32 * cb, v);
+                    if (d1) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(d1 + (size_t)row * D + 32 * cb + i) =
+                                make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    }
+                }
                 uint32_t hw[16], lw[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) split_pair(v[2 * e], v[2 * e + 1], hw[e], lw[e]);
@@ -456,7 +492,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             const bool single = R.single != 0;
             const float qk0 = R.qk0;
             const size_t tstride = (size_t)H * D;
-            OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)(o_row0 + R.begin) * tstride + (size_t)h * D + row;
+            const bool vec = p.o_vec16 != 0;
+            OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)(o_row0 + R.begin) * tstride + (size_t)h * D +
+                       (vec ? 32 * lq : row);
+            OutT* stg = reinterpret_cast<OutT*>(smem + OFF_OST + lq * 2048);
+            constexpr int kTok = 2048 / (32 * (int)sizeof(OutT));   // tokens per staged tile: 32 bf16, 16 fp32
+            constexpr int kSeg = 32 * (int)sizeof(OutT) / 16;        // 16-byte pieces per token and warp
 #pragma unroll 1
             for (int cb = 0; cb < 2 && 32 * cb < n; ++cb) {
                 float v[32], rs[32];
@@ -475,14 +516,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 for (int j = 1; j < 32; ++j) v[j] *= rs[j];
                 if (cb == 1) v[0] *= rs[0];
                 const int m = n - 32 * cb;
+                if (vec) {
+                    // through a [tokens][32 rows] tile: each token's 32 rows leave as whole 16-byte pieces
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (j < m) {
-                        OutT* op = ob + (size_t)(32 * cb + j) * tstride;
-                        if constexpr (OUT_BF16)
-                            *op = __float2bfloat16_rn(v[j]);
-                        else
-                            *op = v[j];
+                    for (int ps = 0; ps < 32 / kTok; ++ps) {
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < kTok; ++i) {
+                            if constexpr (OUT_BF16)
+                                stg[i * 32 + lane] = __float2bfloat16_rn(v[ps * kTok + i]);
+                            else
+                                stg[i * 32 + lane] = v[ps * kTok + i];
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < kTok * kSeg / 32; ++k) {
+                            const int e = 32 * k + lane, i = e / kSeg, u = e % kSeg;
+                            const int t = ps * kTok + i;
+                            if (t < m)
+                                *reinterpret_cast<uint4*>(ob + (size_t)(32 * cb + t) * tstride + u * (16 / sizeof(OutT))) =
+                                    *reinterpret_cast<const uint4*>(stg + i * 32 + u * (16 / sizeof(OutT)));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j < m) {
+                            OutT* op = ob + (size_t)(32 * cb + j) * tstride;
+                            if constexpr (OUT_BF16)
+                                *op = __float2bfloat16_rn(v[j]);
+                            else
+                                *op = v[j];
+                        }
                     }
                 }
             }
@@ -506,7 +571,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         tmem_st_wait();
         bool ok = group_wait(&bar_ring[0], 0, tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit);
         if (ok) {
-            split_state(ring[0]);
+            split_state(ring[0], nullptr);
             tc_fence_before();
             mbar_arrive(bar_split);
             float u0_prev = 0.f;
@@ -548,7 +613,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 if (!group_wait(bar_st, (uint32_t)(j & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
                 tc_fence_after();
                 const bool fold = R.fold != 0, last = R.last != 0;
-                if (fold) fold_state(R);
+                if (fold && last) fold_state(R);   // otherwise folded in the next split
                 u0_prev = u0;
                 if (last) {
                     if (rd) {
@@ -565,7 +630,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     break;
                 const Ring& Rn = ring[jn % kRing];
                 if (tid == 0 && Rn.next_len > 0 && allowed(j + 2)) issue_kq(j + 2, Rn.next_begin);
-                split_state(Rn);
+                split_state(Rn, &R);
                 tc_fence_before();
                 mbar_arrive(bar_split);
             }
@@ -604,29 +669,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 gb1 = __ldg(p.beta + gbase + (size_t)(lane + 32) * H);
             }
         };
-        auto prefix = [&](float a0, float a1, float& g0, float& g1) {   // inclusive products over the warp
-            g0 = a0;
-            g1 = a1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float x0 = __shfl_up_sync(0xffffffffu, g0, off);
-                const float x1 = __shfl_up_sync(0xffffffffu, g1, off);
-                if (lane >= off) {
-                    g0 *= x0;
-                    g1 *= x1;
-                }
-            }
-            g1 *= __shfl_sync(0xffffffffu, g0, 31);
-        };
         // schedule and scalars of chunk jj (window g_win), published in ring[jj % kRing]
         auto compute_chunk = [&](int jj) {
             float a0 = ga0, a1 = ga1, b0 = gb0, b1 = gb1;
             float g0, g1;
-            prefix(a0, a1, g0, g1);
-            const unsigned m0 = __ballot_sync(0xffffffffu, g0 < kGammaFloor);
-            const unsigned m1 = __ballot_sync(0xffffffffu, g1 < kGammaFloor);
-            const int first = m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : C);
+            gate_prefix(a0, a1, g0, g1, lane);
             int n = g_win.len;
+            const int first = gamma_first(g0, g1);
             if (first < n) {
                 n = first > 0 ? first : 1;
                 if (lane >= n) {
@@ -637,7 +686,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     a1 = 1.f;
                     b1 = 0.f;
                 }
-                prefix(a0, a1, g0, g1);
+                gate_prefix(a0, a1, g0, g1, lane);
             }
             const float gfirst = __shfl_sync(0xffffffffu, g0, 0);
             const float glast = __shfl_sync(0xffffffffu, n > 32 ? g1 : g0, (n - 1) & 31);
@@ -695,6 +744,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             if (lane == 0 && allowed(0)) {
                 issue_kq(0, 0);
                 issue_v(0, 0);
+                if (PRE_T) issue_t(0, 0);
             }
             compute_chunk(0);
             if (lane == 0 && ring[0].next_len > 0 && allowed(1)) issue_kq(1, ring[0].next_begin);
@@ -728,6 +778,112 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         };
         bool staged = stage_kq(0);
 
+        if constexpr (PRE_T) {
+            // T of every chunk was computed by the first passes: the group converts it and serves the
+            // chain as before (P, -sigma_0 W, padded tiles)
+            for (int j = 0; staged; ++j) {
+                const Ring& R = ring[j % kRing];
+                const int n = R.n;
+                const bool single = R.single != 0;
+                const bool last = R.last != 0;
+                const float* ps = psc + (j & 1) * 4 * C;
+                if (pw == 3 && !last) compute_chunk(j + 1);   // the gate warp runs one chunk ahead
+
+                // ---- this chunk's V (rows past the chunk zeroed) ----
+                if (!group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                if (n < C) {
+                    const int nz = C - n;
+                    for (int i = ptid; i < 2 * nz * 8; i += NPREP) {
+                        const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;
+                        *reinterpret_cast<uint4*>(smem + OFF_V + part * 8192 + (n + rz) * 128 + seg * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                // ---- T -> T diag(beta gamma), T diag(beta) as bf16 hi/lo K-major operands; rows past the
+                //      chunk (later tokens' T rows) become zero ----
+                if (!group_wait(bar_t, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                {
+                    const float* Tt = reinterpret_cast<const float*>(smem + OFF_LF);
+                    const float* sg_bg = ps + 2 * C;
+                    const float* sg_b = ps + 3 * C;
+                    const int t = ptid >> 2, c0 = 16 * (ptid & 3);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int cc = c0 + 8 * q;
+                        uint32_t h1[4] = {0u, 0u, 0u, 0u}, l1[4] = {0u, 0u, 0u, 0u};
+                        uint32_t h2[4] = {0u, 0u, 0u, 0u}, l2[4] = {0u, 0u, 0u, 0u};
+                        if (t < n) {
+                            const float4 x0 = *reinterpret_cast<const float4*>(Tt + t * C + cc);
+                            const float4 x1 = *reinterpret_cast<const float4*>(Tt + t * C + cc + 4);
+                            const float4 a0 = *reinterpret_cast<const float4*>(sg_bg + cc);
+                            const float4 a1 = *reinterpret_cast<const float4*>(sg_bg + cc + 4);
+                            const float4 b0 = *reinterpret_cast<const float4*>(sg_b + cc);
+                            const float4 b1 = *reinterpret_cast<const float4*>(sg_b + cc + 4);
+                            split_pair(x0.x * a0.x, x0.y * a0.y, h1[0], l1[0]);
+                            split_pair(x0.z * a0.z, x0.w * a0.w, h1[1], l1[1]);
+                            split_pair(x1.x * a1.x, x1.y * a1.y, h1[2], l1[2]);
+                            split_pair(x1.z * a1.z, x1.w * a1.w, h1[3], l1[3]);
+                            split_pair(x0.x * b0.x, x0.y * b0.y, h2[0], l2[0]);
+                            split_pair(x0.z * b0.z, x0.w * b0.w, h2[1], l2[1]);
+                            split_pair(x1.x * b1.x, x1.y * b1.y, h2[2], l2[2]);
+                            split_pair(x1.z * b1.z, x1.w * b1.w, h2[3], l2[3]);
+                        }
+                        const uint32_t o = sw128(t, cc);
+                        *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+                        *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+                        *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                        *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+                    }
+                }
+                proxy_fence();
+                group_sync(BAR_PREP, NPREP);
+                if (leader) {
+                    mbar_arrive(bar_wuin);
+                    if (!last && allowed(j + 1)) issue_t(j + 1, R.next_begin);   // the T area is free again
+                }
+
+                // ---- W^T = K^T T1^T, U~^T = V^T T2^T; then -sigma_0 W^T as the MN-major B operand: first, as
+                //      the chain's next U^T waits for it, while P waits for the previous readout ----
+                if (!group_wait(bar_wu, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                tc_fence_after();
+                if (leader && !last && allowed(j + 1)) issue_v(j + 1, R.next_begin);   // the V buffer is free again
+                {
+                    const float f = -R.sigma0;
+                    float v[32];
+                    tmem_ld32(trow + T_W + 32 * half, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= f;
+                    st_split32(smem + OFF_WH, smem + OFF_WL, row, 32 * half, v);
+                }
+                proxy_fence();
+                tc_fence_before();
+                mbar_arrive(bar_wready);
+
+                // ---- P = mask(q_t . k_s) from the Q rows of [K; Q] K^T, once the chain's previous U''^T P^T is
+                //      done; then the next chunk's K/Q tiles ----
+                if (rd) {
+                    if (j > 0 && !group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
+                        break;
+                    if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                    tc_fence_after();
+                    if (lq >= 2) {
+                        float v[32];
+                        tmem_ld32(trow + T_G + 32 * half, v);
+                        const int t = row - 64, s0 = 32 * half;
+                        if (single && t == 0 && half == 0) ring[j % kRing].qk0 = v[0];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = (!single && s0 + i <= t) ? v[i] : 0.f;
+                        st_split32(smem + OFF_PH, smem + OFF_PL, t, s0, v);
+                    }
+                    proxy_fence();
+                    tc_fence_before();
+                    mbar_arrive(bar_pready);
+                }
+                if (!last && !(staged = stage_kq(j + 1))) break;
+
+                if (last) break;
+            }
+        } else {
         for (int j = 0; staged; ++j) {
             const Ring& R = ring[j % kRing];
             const int n = R.n;
@@ -959,9 +1115,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 
             if (last) break;
         }
+        }
     } else if (lane == 0) {
         // ============================ MMA issue (warp 12, one lane) ============================
-        // Two streams, each in its own order: prep G_j, WU_j (served first) and chain U_j, O1_j, St_j, O2_j.
+        // Two streams, each in its own order: prep G_j, WU_j and chain U_j, O1_j, St_j, O2_j; the prep stream
+        // is served first when the prep group bounds the pipeline (T computed here), else the chain.
         // An item is issued once the mbarriers of its operands have fired; a stream ends after its last chunk.
         int jc = 0, sc = 0, jp = 0, sp = 0;
         bool chain_done = false, prep_done = false;
@@ -970,18 +1128,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         const uint32_t id128b = idesc(128, false, true);
         while (!(chain_done && prep_done)) {
             bool progressed = false;
+            auto serve_prep = [&]() {
             if (!prep_done) {
                 const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
                 if (sp == 0 && mbar_test(bar_gin, jp & 1)) {
                     tc_fence_after();
-                    // [K; Q] K^T: its K rows give L, its Q rows P
+                    // [K; Q] K^T: its K rows give L, its Q rows P (with T given, only P is needed)
+                    if (!PRE_T || rd) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64,
+                                    kk > 0);
+                        }
+                        umma_commit(bar_g);
+                        ++cnt[2];
                     }
-                    umma_commit(bar_g);
-                    ++cnt[2];
                     sp = 1;
                     progressed = true;
                 }
@@ -1008,6 +1170,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     }
                 }
             }
+            };
+            auto serve_chain = [&]() {
             if (!chain_done) {
                 const Ring& R = ring[jc % kRing];
                 const uint32_t inKQ = sbase + OFF_KQ + (jc & 1) * 32768;
@@ -1092,6 +1256,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     }
                 }
             }
+            };
+            // with T computed beforehand the state chain is the critical path: its products go first
+            if (PRE_T) {
+                serve_chain();
+                serve_prep();
+            } else {
+                serve_prep();
+                serve_chain();
+            }
             if (progressed) {
                 t_last = global_ns();
             } else {
@@ -1115,6 +1288,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             if (c >= 0) drain_phase(&bar_kq[b], (uint32_t)((c >> 1) & 1), drain_limit);
         }
         if (cnt[1] > 0) drain_phase(bar_v, (uint32_t)((cnt[1] - 1) & 1), drain_limit);
+        if (cnt[7] > 0) drain_phase(bar_t, (uint32_t)((cnt[7] - 1) & 1), drain_limit);
         for (int i = 0; i < 5; ++i)
             if (cnt[2 + i] > 0) drain_phase(&bars[3 + i], (uint32_t)((cnt[2 + i] - 1) & 1), drain_limit);
         atomicOr(p.status, STATUS_TIMEOUT);
@@ -1124,17 +1298,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(512));
 }
 
-template <bool OUT_BF16, bool READOUT>
+template <bool OUT_BF16, bool READOUT, bool PRE_T>
 cudaError_t launch_chunk_tc(const Params& p, int grid, cudaStream_t stream) {
-    auto kern = gdn_chunk_tc_kernel<OUT_BF16, READOUT>;
+    auto kern = gdn_chunk_tc_kernel<OUT_BF16, READOUT, PRE_T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, NTHREADS, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
-// instantiated in inst_chunk_tc.cu
-cudaError_t launch(const Params& p, int grid, bool readout, bool out_bf16, cudaStream_t stream);
+// instantiated in inst_chunk_tc.cu; pre_t: T of every chunk is in p.t_rows (two-pass path)
+cudaError_t launch(const Params& p, int grid, bool readout, bool out_bf16, bool pre_t, cudaStream_t stream);
+// the first passes of the two-pass path (gdn_tprep.cu): the chunk schedule of every (job, head) into
+// p.chunk_beg / p.chunk_cnt, then T of every chunk into p.t_rows; n_streams = jobs x heads
+cudaError_t launch_schedule(const Params& p, int n_streams, cudaStream_t stream);
+cudaError_t launch_tprep(const Params& p, int n_streams, cudaStream_t stream);
 
 }  // namespace tc
 }  // namespace gdn

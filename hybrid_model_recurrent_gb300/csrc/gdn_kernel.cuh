@@ -65,7 +65,7 @@ struct Job {
     int32_t len;            // tokens
     int32_t ck_begin;       // first entry of the launch's checkpoint table
     int32_t ck_count;       // entries for this job
-    int32_t pad_;
+    int32_t t_row0;         // two-pass chunked path: first row of this job's block of T rows (H x len rows)
 };
 static_assert(sizeof(Job) == 64, "Job layout");
 
@@ -91,10 +91,17 @@ struct Params {
     int32_t ctas_per_head;  // dv / rows_per_cta
     int32_t n_jobs;
     int32_t stall_after;    // testing hook: stop issuing input copies after this many chunks (-1: off)
-    int32_t pad_;
+    int32_t o_vec16;        // o is 16-byte aligned: the chunked kernel may write it in 16-byte pieces
+    // two-pass chunked path only: the chunk schedule and T = (I + L)^-1 of every chunk, computed by
+    // parallel passes before the state scan (workspace buffers)
+    CUtensorMap tm_t;       // t_rows as [rows, 64] fp32, box (64, 64)
+    int32_t* chunk_beg;     // [rows]: chunk c of (job, head) starts at token chunk_beg[t_row0 + head * len + c]
+    int32_t* chunk_cnt;     // [n_jobs, H]: chunks of (job, head)
+    float* t_rows;          // [rows, 64]: row t_row0 + head * len + t is row t - begin of its chunk's T
     Job jobs[kMaxJobs];
     Ckpt ckpts[kMaxCkpts];
 };
+static_assert(sizeof(Params) <= 32764, "kernel parameter block");
 
 // ------------------------------------------------------------------------------------
 // PTX helpers
@@ -152,6 +159,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, in
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
 }
 __device__ __forceinline__ void fence_barrier_init() {

@@ -29,7 +29,10 @@
  *    only then.
  *  - The caller owns every buffer.  The library allocates no device memory;
  *    it needs a small caller-provided workspace (gdn_workspace_size bytes,
- *    16-byte aligned) that carries a sticky device status word.
+ *    16-byte aligned) that carries a sticky device status word.  A larger
+ *    workspace (gdn_workspace_size_two_pass bytes) lets the chunked scan
+ *    precompute the per-chunk matrices of every chunk in parallel first
+ *    (GDN_ALGO_CHUNKED_TWO_PASS), which AUTO then prefers.
  *  - Errors: a non-GDN_OK status.  Invalid arguments are detected on the
  *    host before anything is enqueued; outputs are then untouched.  A
  *    kernel-side failure (a bounded wait that ran out) is reported later by
@@ -64,8 +67,9 @@ typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 /* Which kernel runs the scan.  All compute the same recurrence in fp32 state
  * precision; they differ in rounding order only.
- *  GDN_ALGO_AUTO         GDN_ALGO_CHUNKED when supported (d_k = d_v = 128, bf16
- *                        q/k/v), otherwise per-token
+ *  GDN_ALGO_AUTO         when supported (d_k = d_v = 128, bf16 q/k/v)
+ *                        GDN_ALGO_CHUNKED_TWO_PASS if the workspace is large
+ *                        enough for it, else GDN_ALGO_CHUNKED; otherwise per-token
  *  GDN_ALGO_PER_TOKEN    token by token on the FP32 pipes (any supported size)
  *  GDN_ALGO_CHUNKED      chunks of up to 64 tokens (WY / UT-transform form) on the
  *                        5th-generation tensor cores (tcgen05, accumulators and
@@ -77,12 +81,21 @@ typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  *                        chunks only: the decay product over one chunk must stay
  *                        above 2^-126 (alpha^64 > 1.2e-38), else results are not
  *                        finite.
- * The two chunked algorithms return GDN_ERR_UNSUPPORTED for other sizes. */
+ *  GDN_ALGO_CHUNKED_TWO_PASS  the chunks of GDN_ALGO_CHUNKED (same chunk ends), in
+ *                        three launches: the chunk schedule of every (range, head),
+ *                        T = (I + L)^-1 of every chunk at once on every SM, then the
+ *                        tcgen05 state scan, which no longer waits for T.  Needs a
+ *                        workspace of gdn_workspace_size_two_pass bytes for the
+ *                        call (GDN_ERR_INVALID_ARG with a smaller one).
+ * The chunked algorithms return GDN_ERR_UNSUPPORTED for other sizes.  Calls whose
+ * results are compared bit for bit (a resume against its prefill) must use the
+ * same algorithm: the chunked ones differ from each other in rounding order. */
 typedef enum gdn_algo {
     GDN_ALGO_AUTO = 0,
     GDN_ALGO_PER_TOKEN = 1,
     GDN_ALGO_CHUNKED = 2,
-    GDN_ALGO_CHUNKED_MMA = 3
+    GDN_ALGO_CHUNKED_MMA = 3,
+    GDN_ALGO_CHUNKED_TWO_PASS = 4
 } gdn_algo;
 
 typedef struct gdn_problem {
@@ -356,6 +369,15 @@ gdn_status gdn_expected_recompute(const int64_t* weights, int64_t N, const int64
 
 /* Bytes of workspace every device entry point needs. */
 size_t gdn_workspace_size(void);
+
+/* Bytes of workspace with which a call can use GDN_ALGO_CHUNKED_TWO_PASS:
+ * `tokens` = tokens scanned by the call summed over its ranges (prefill: T;
+ * resume: the sum of the probe depths bounds it; tail replay: the sum of the
+ * tails, plus the sum of m when S_a is given), `num_ranges` = ranges scanned
+ * (sequences, probes; twice the sequences for a replay with S_a).  It holds
+ * the status word, the chunk schedule and T = (I + L)^-1 (64 fp32 per token
+ * and head).  0 for negative arguments or more than 2^31 token-heads. */
+size_t gdn_workspace_size_two_pass(int64_t tokens, int32_t num_heads, int32_t num_ranges);
 
 /* Zero the sticky status word of a workspace (enqueued on stream). */
 gdn_status gdn_clear_status(void* workspace, size_t ws_bytes, gdn_stream_t stream);

@@ -104,11 +104,15 @@ def test_prefill_rejects_bad_arguments(L):
     assert prefill(L, _prob(cu=(0, 10, 5))[0]) == E           # decreasing cu_seqlens
     assert prefill(L, _prob(cu=(1, 10, 30))[0]) == E           # cu_seqlens[0] != 0
     assert prefill(L, _prob(qkv=7)[0]) == E
-    assert prefill(L, _prob(algo=4)[0]) == E                    # unknown algorithm
+    assert prefill(L, _prob(algo=5)[0]) == E                    # unknown algorithm
     assert prefill(L, _prob(algo=-1)[0]) == E
-    for a in (gdn.ALGO["chunked"], gdn.ALGO["chunked_mma"]):
+    for a in (gdn.ALGO["chunked"], gdn.ALGO["chunked_mma"], gdn.ALGO["two_pass"]):
         assert prefill(L, _prob(algo=a)[0]) == U                # chunked needs d_k = d_v = 128 and bf16
         assert prefill(L, _prob(dk=128, dv=128, qkv=gdn.GDN_F32, algo=a)[0]) == U
+    # the two-pass path needs its larger workspace (30 tokens x 2 heads, 2 sequences here)
+    pr2, _k2 = _prob(dk=128, dv=128, algo=gdn.ALGO["two_pass"])
+    need = L.gdn_workspace_size_two_pass(30, 2, 2)
+    assert prefill(L, pr2) == E and prefill(L, pr2, wsb=need - 1) == E
     assert prefill(L, pr, k=None) == E
     assert prefill(L, pr, q=None) == E                          # readout requested without q
     assert prefill(L, pr, k=_vp(0x1008)) == E                   # k not 16-byte aligned
@@ -133,9 +137,26 @@ def test_prefill_valid_call_without_gpu_reports_cuda_error(L):
     pr, _keep = _prob()
     # arguments are valid: the library gets as far as CUDA, which is absent here
     assert prefill(L, pr, pos=[5, 10, 7], cu=[0, 2, 3]) == gdn.GDN_ERR_CUDA
+    big = L.gdn_workspace_size_two_pass(30, 2, 2)
     for a in gdn.ALGO.values():
         pr2, _k2 = _prob(dk=128, dv=128, algo=a)
-        assert prefill(L, pr2, pos=[5, 10, 7], cu=[0, 2, 3]) == gdn.GDN_ERR_CUDA
+        assert prefill(L, pr2, pos=[5, 10, 7], cu=[0, 2, 3], wsb=big) == gdn.GDN_ERR_CUDA
+
+
+def test_two_pass_workspace_size(L):
+    base = L.gdn_workspace_size()
+    f = L.gdn_workspace_size_two_pass
+    assert f(0, 1, 0) == base
+    # status word, chunk counts (4 B per range and head), chunk starts (4 B per token and head), T rows
+    # (64 fp32 per token and head), each part 256-byte aligned
+    up = lambda x: (x + 255) // 256 * 256
+    for T, H, R in ((30, 2, 2), (8192 * 8, 16, 8), (1, 1, 1), (1000, 3, 7)):
+        cnt = base
+        beg = up(cnt + 4 * R * H)
+        t = up(beg + 4 * T * H)
+        assert f(T, H, R) == t + 256 * T * H
+    assert f(-1, 1, 1) == 0 and f(1, 0, 1) == 0 and f(1, 1, -1) == 0
+    assert f(1 << 31, 1, 1) == 0 and f(1 << 27, 16, 1) == 0     # more than 2^31 - 1 token-heads
 
 
 def test_resume_and_replay_reject_bad_arguments(L):

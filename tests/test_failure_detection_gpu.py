@@ -15,7 +15,7 @@ from parity_util import assert_close
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "two_pass"])
 def test_wait_limit_expiry_is_reported_and_recoverable(algo):
     gdn.build()
     w = synth.Workload("fd", [4096, 3000], 8, 128, 128, torch.bfloat16, torch.bfloat16, 0.95, 1.0, "uniform",
@@ -24,7 +24,8 @@ def test_wait_limit_expiry_is_reported_and_recoverable(algo):
     ck = [[1024, 4096], [512]]
     ref = gdn.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, w.cu_seqlens, ckpt_pos=ck, algo=algo)
     torch.cuda.synchronize()
-    ws = torch.zeros(int(gdn.lib().gdn_workspace_size()), dtype=torch.uint8, device="cuda")
+    nbytes = gdn.lib().gdn_workspace_size_two_pass(7096, 8, 2) if algo == "two_pass" else gdn.lib().gdn_workspace_size()
+    ws = torch.zeros(int(nbytes), dtype=torch.uint8, device="cuda")
     try:
         gdn.set_wait_limit_ns(20_000_000)   # 20 ms
         gdn.debug_stall_after(3)

@@ -107,6 +107,7 @@ def test_tiny_prefill_resume_replay():
     (64, 64, torch.bfloat16, torch.bfloat16, "auto"), (64, 64, torch.bfloat16, torch.float32, "auto"),
     (128, 128, torch.bfloat16, torch.bfloat16, "per_token"), (128, 128, torch.bfloat16, torch.bfloat16, "chunked"),
     (128, 128, torch.bfloat16, torch.float32, "chunked"), (128, 128, torch.bfloat16, torch.bfloat16, "chunked_mma"),
+    (128, 128, torch.bfloat16, torch.bfloat16, "two_pass"), (128, 128, torch.bfloat16, torch.float32, "two_pass"),
     (128, 128, torch.float32, torch.float32, "auto"),
     (32, 32, torch.bfloat16, torch.float32, "auto"), (128, 64, torch.bfloat16, torch.float32, "auto"),
     (64, 128, torch.float32, torch.bfloat16, "auto"), (32, 128, torch.bfloat16, torch.bfloat16, "auto"),
@@ -140,7 +141,7 @@ def test_ragged_prefill_with_initial_state(dk, dv, dtype, out, algo):
 
 
 @pytest.mark.parametrize("dk,dv,algo", [(128, 128, "per_token"), (128, 128, "chunked"), (128, 128, "chunked_mma"),
-                                        (64, 32, "auto")])
+                                        (128, 128, "two_pass"), (64, 32, "auto")])
 def test_ragged_replay_twin_and_readout(dk, dv, algo):
     lens = [200, 71, 5, 64]
     H = 4
@@ -176,7 +177,7 @@ def test_ragged_replay_twin_and_readout(dk, dv, algo):
             assert_close(rp["S_hat"][b, h], o_["S_hat"], f"S_hat(no twin) b={b} h={h}")
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma", "two_pass"])
 def test_resume_from_seeded_checkpoints(algo):
     """Resume with checkpoint states drawn by the generator (fed to both sides)."""
     lens = [300, 130]
@@ -221,7 +222,7 @@ def _small_alpha_inputs(seed, lens, H):
     return w, synth.Inputs(inp.q, inp.k, inp.v, alpha, inp.beta)
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "two_pass"])
 def test_small_alpha_gates(algo):
     """alpha down to 1e-30 (the bottom of the documented range), with checkpoints and a resume."""
     lens = [300, 129]
@@ -268,7 +269,7 @@ def test_small_alpha_gates(algo):
                 check_output(rs["o"][lo:hi, h], o_["o"], f"small-alpha resume o probe {i} h={h}")
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "two_pass"])
 def test_placement_feeds_prefill_and_resume(algo):
     """Checkpoints chosen by the placement programme ("Sparse prefix caching ...", Theorem 2) for a
     seeded depth distribution drive gdn_prefill_ckpt; resume probes at depths drawn from the same
@@ -315,7 +316,7 @@ def test_placement_feeds_prefill_and_resume(algo):
 # ---------------------------------------------------------------------------------------------
 # invariants on the GPU
 # ---------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma", "two_pass"])
 def test_identity_gates_leave_state_unchanged(algo):
     lens = [77]
     H, dk, dv = 2, 128, 128
@@ -330,7 +331,7 @@ def test_identity_gates_leave_state_unchanged(algo):
     assert torch.equal(r["S_final"].cpu(), S0), "alpha = 1, beta = 0 must leave S unchanged (bitwise)"
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma", "two_pass"])
 def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic(algo):
     """Resume from the deepest stored checkpoint c_j <= d reproduces, bit for bit,
     the state at d of a full run that stores the same checkpoints plus d.  (Each
@@ -400,7 +401,7 @@ def _host_head(inp, t0, t1, h, with_q=True):
     return q, inp.k[t0:t1, h].cpu(), inp.v[t0:t1, h].cpu(), inp.alpha[t0:t1, h].cpu(), inp.beta[t0:t1, h].cpu()
 
 
-@pytest.mark.parametrize("algo", ["auto", "per_token"])
+@pytest.mark.parametrize("algo", ["auto", "chunked", "per_token"])
 def test_full_prefill_workload_sampled(algo):
     """8 x 16 heads, N = 8192, bf16, 16 equally spaced checkpoints: full run, sampled oracle."""
     w = synth.workload("prefill")

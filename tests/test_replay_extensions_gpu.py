@@ -35,7 +35,7 @@ def _dev(inp):
     return synth.Inputs(inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV), inp.alpha.to(DEV), inp.beta.to(DEV))
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked"])
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "two_pass"])
 def test_replay_k_matches_r_based_replay_and_oracle(algo):
     lens = [300, 129, 64]
     H = 2
