@@ -115,18 +115,18 @@ gdn_status check_workspace(void* ws, size_t bytes) {
 }
 
 // Workspace of the two-pass chunked path: after the status word, the chunk counts [streams], the chunk
-// starts [rows] and T [rows][64] fp32, where rows = sum over the call's ranges of len x H.
+// starts [rows] and the T operands [4][rows][64] bf16, where rows = sum over the call's ranges of len x H.
 struct TwoPassLayout {
     size_t cnt_off, beg_off, t_off, total;
 };
-constexpr int64_t kMaxTwoPassRows = ((int64_t)1 << 31) - 1;
+constexpr int64_t kMaxTwoPassRows = ((int64_t)1 << 29) - gdn::tc::C;   // 4 planes of rows keep copy coordinates in int32
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 TwoPassLayout two_pass_layout(int64_t rows, int64_t streams) {
     TwoPassLayout l;
     l.cnt_off = kWorkspaceBytes;
     l.beg_off = round_up(l.cnt_off + 4 * (size_t)streams, 256);
     l.t_off = round_up(l.beg_off + 4 * (size_t)rows, 256);
-    l.total = l.t_off + (size_t)rows * gdn::tc::C * sizeof(float);
+    l.total = l.t_off + (size_t)rows * 4 * gdn::tc::C * 2;
     return l;
 }
 
@@ -247,15 +247,16 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
         unsigned char* ws = reinterpret_cast<unsigned char*>(L.status);
         prm->chunk_cnt = reinterpret_cast<int32_t*>(ws + lay.cnt_off);
         prm->chunk_beg = reinterpret_cast<int32_t*>(ws + lay.beg_off);
-        prm->t_rows = reinterpret_cast<float*>(ws + lay.t_off);
+        prm->t_ops = ws + lay.t_off;
+        prm->t_rows = (int32_t)std::max<int64_t>(rows, 1);
         EncodeTiledFn enc = encode_fn();
         if (!enc) return GDN_ERR_CUDA;
-        cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)std::max<int64_t>(rows, 1)};
-        cuuint64_t strides[1] = {(cuuint64_t)(C * sizeof(float))};
+        cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(4 * (int64_t)prm->t_rows)};
+        cuuint64_t strides[1] = {(cuuint64_t)(C * 2)};
         cuuint32_t box[2] = {(cuuint32_t)C, (cuuint32_t)C};
         cuuint32_t estr[2] = {1u, 1u};
-        if (enc(&prm->tm_t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, prm->t_rows, dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        if (enc(&prm->tm_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, prm->t_ops, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return GDN_ERR_CUDA;
     }

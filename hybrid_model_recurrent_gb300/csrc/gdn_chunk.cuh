@@ -676,7 +676,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_kernel(const __grid_con
 template <bool OUT_BF16, bool READOUT>
 cudaError_t launch_chunk(const Params& p, int grid, cudaStream_t stream) {
     auto kern = gdn_chunk_kernel<OUT_BF16, READOUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static std::atomic<int> optin[kMaxOptinDevices];
+    cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), kSmemBytes, optin);
     if (e != cudaSuccess) return e;
     kern<<<grid, NTHREADS, kSmemBytes, stream>>>(p);
     return cudaGetLastError();

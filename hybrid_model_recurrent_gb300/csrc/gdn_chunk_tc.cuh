@@ -47,8 +47,10 @@
 // wait that runs out ends every loop without leaving a named barrier half-entered.
 //
 // TMEM (512 columns x 128 lanes of 32 bit):
-//   [0,128) St   [128,192) U^T   [192,256) O^T   [256,320) [K; Q] K^T   [320,384) W^T
+//   [0,128) St   [128,192) U^T   [192,256) W^T   [256,320) O^T   [320,384) [K; Q] K^T
 //   [384,448) St hi (bf16 pairs)   [448,512) St lo
+// W^T directly follows U^T so that U^T += St (-sigma_0 W)^T takes [W_hi | W_lo] as one N = 128 operand:
+// the W columns, zeroed once W is read out, then collect the S_hi W_lo^T half, added when U is read.
 #pragma once
 
 #include <climits>
@@ -99,14 +101,16 @@ constexpr int OFF_PSC = 218368;        // fp32 prep scalars [2][4][64]: gamma, 1
 constexpr int OFF_RING = 220416;       // Ring[kRing]
 constexpr int OFF_BAR = OFF_RING + kRing * 576;
 constexpr int kBarBytes = 256;
-constexpr int OFF_OST = OFF_BAR + kBarBytes;   // 4 x 2 KB: readout staging, one [tokens][32 rows] tile per chain warp
+constexpr int OFF_OST = OFF_BAR + kBarBytes;   // 8 KB: readout staging, a [tokens][32 rows] tile per reading warp
+constexpr int OFF_U0 = OFF_LF + C * C * 4;     // two-pass: fp32 [2][128] u_1 of single-token chunks (after the T tile)
+static_assert(OFF_U0 + 2 * 128 * 4 <= OFF_LD, "u_1 buffer inside the L area");
 constexpr int kSmemBytes = OFF_OST + 4 * 2048 + 1024;
 static_assert(kSmemBytes <= 232448, "227 KB of shared memory per block");
 constexpr int kLdF = 68;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(OFF_PSC + 2 * 4 * C * 4 == OFF_RING, "scalar area");
 
-constexpr uint32_t T_S = 0, T_U = 128, T_O = 192, T_G = 256, T_W = 320, T_SH = 384, T_SL = 448;
+constexpr uint32_t T_S = 0, T_U = 128, T_W = 192, T_O = 256, T_G = 320, T_SH = 384, T_SL = 448;
 constexpr float kGammaFloor = 0x1p-32f;   // smallest in-chunk decay product
 constexpr float kSigmaFloor = 0x1p-40f;   // fold the running scale into the state below this
 
@@ -199,6 +203,22 @@ __device__ __forceinline__ void st_split32(unsigned char* th, unsigned char* tl,
         *reinterpret_cast<uint4*>(th + sw128(row, c0 + 8 * q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *reinterpret_cast<uint4*>(tl + sw128(row, c0 + 8 * q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
+}
+// ldmatrix (four / two 8x8 b16 matrices) and mma.sync m16n8k16 (row.col, bf16 -> fp32)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 // x = hi + lo, both tf32 (10 explicit mantissa bits each)
 __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         mbar_init(bar_wready, NPREP);
         mbar_init(bar_pready, NPREP);
         mbar_init(bar_split, NCHAIN);
-        mbar_init(bar_ofree, NCHAIN);
+        mbar_init(bar_ofree, PRE_T ? NPREP : NCHAIN);   // the group that reads O out
         mbar_init(bar_ufree, NCHAIN);
         for (int i = 0; i < kRing; ++i) mbar_init(&bar_ring[i], 32);
         mbar_init(bar_t, 1);
@@ -380,6 +400,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     tc_fence_after();
     const uint32_t tbase = *tslot;
     const uint32_t trow = tbase + ((uint32_t)(32 * lq) << 16);   // this warp's lane quarter
+    // W follows U in TMEM, so U^T += St [W_hi | W_lo]^T runs as one N = 128 product per k step whose second
+    // half (zeroed once W is read) is added when U is read
+    constexpr uint32_t TW = T_W, TO = T_O, TG = T_G;
 
     auto allowed = [&](int c) { return p.stall_after < 0 || c < p.stall_after; };   // testing hook
     auto issue_kq = [&](int c, int pos) {
@@ -394,11 +417,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         tma_load_3d(dst + 16384 + 8192, &p.tm_q, 64, h, t0, &bar_kq[buf]);
         atomicMax(&cnt[0], c + 1);
     };
-    // T of chunk c (starting at token pos) from the rows the first passes wrote, into the L area
+    // T diag(beta gamma), T diag(beta) (bf16 hi, lo) of chunk c (starting at token pos) from the rows the
+    // first passes wrote, straight into the operand tiles (the copy's 128-byte swizzle is the MMA layout)
     auto issue_t = [&](int c, int pos) {
         proxy_fence();
-        mbar_arrive_expect_tx(bar_t, (uint32_t)(C * C * 4));
-        tma_load_2d(smem + OFF_LF, &p.tm_t, 0, job.t_row0 + h * len + pos, bar_t);
+        mbar_arrive_expect_tx(bar_t, 4u * 8192u);
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl)
+            tma_load_2d(smem + OFF_T1H + pl * 8192, &p.tm_t, 0, pl * p.t_rows + job.t_row0 + h * len + pos, bar_t);
         atomicMax(&cnt[7], c + 1);
     };
     auto issue_v = [&](int c, int pos) {
@@ -421,6 +447,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         }
     } else if (warp < 4) {
         // ============================ chain group ============================
+        // state rows 32 lq .. 32 lq + 31, columns c0 .. c0 + 31 (one per lane's v) to dst [d_v][d_k]: through a
+        // 32 x 8 tile per pass so that every store instruction writes whole 32-byte sectors
+        float* dstg = reinterpret_cast<float*>(smem + (PRE_T ? OFF_LD : OFF_OST) + lq * (PRE_T ? 1024 : 2048));
+        auto dump_cols = [&](float* dst, int c0, const float (&v)[32]) {
+#pragma unroll
+            for (int ps = 0; ps < 4; ++ps) {
+                __syncwarp();
+                *reinterpret_cast<float4*>(dstg + lane * 8) =
+                    make_float4(v[8 * ps], v[8 * ps + 1], v[8 * ps + 2], v[8 * ps + 3]);
+                *reinterpret_cast<float4*>(dstg + lane * 8 + 4) =
+                    make_float4(v[8 * ps + 4], v[8 * ps + 5], v[8 * ps + 6], v[8 * ps + 7]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int e = 32 * k + lane, r = e >> 1, hq = e & 1;
+                    *reinterpret_cast<float4*>(dst + (size_t)(32 * lq + r) * D + c0 + 8 * ps + 4 * hq) =
+                        *reinterpret_cast<const float4*>(dstg + r * 8 + 4 * hq);
+                }
+            }
+        };
         // St -> bf16 hi/lo pairs (the A operand of chunk Rn).  First, when the previous chunk Rp asks for it,
         // sigma is folded into St and the folded state dumped (checkpoint); a single small-alpha token then
         // scales St.  One pass over St: the fold costs no second read.
@@ -440,12 +486,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= ff;
                     if (!single) tmem_st32(trow + T_S + 32 * cb, v);
-                    if (d1) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(d1 + (size_t)row * D + 32 * cb + i) =
-                                make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                    }
+                    if (d1) dump_cols(d1, 32 * cb, v);
                 }
                 uint32_t hw[16], lw[16];
 #pragma unroll
@@ -471,18 +512,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= f;
                 tmem_st32(trow + T_S + 32 * cb, v);
-                if (d1) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(d1 + (size_t)row * D + 32 * cb + i) =
-                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                }
-                if (d2) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(d2 + (size_t)row * D + 32 * cb + i) =
-                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                }
+                if (d1) dump_cols(d1, 32 * cb, v);
+                if (d2) dump_cols(d2, 32 * cb, v);
             }
             tmem_st_wait();
         };
@@ -509,7 +540,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     rs[i + 2] = x.z;
                     rs[i + 3] = x.w;
                 }
-                tmem_ld32(trow + T_O + 32 * cb, v);
+                tmem_ld32(trow + TO + 32 * cb, v);
                 if (cb == 0 && single) v[0] = fmaf(qk0, u0, rs[0] * v[0]);
                 else if (cb == 0) v[0] *= rs[0];
 #pragma unroll
@@ -581,9 +612,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 if (rd && j > 0) {
                     if (!group_wait(bar_o, (uint32_t)((j - 1) & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
                     tc_fence_after();
-                    readout(ring[(j - 1) % kRing], u0_prev);
-                    tc_fence_before();
-                    mbar_arrive(bar_ofree);
+                    if (!PRE_T) {   // with T given the prep group reads O out; U''^T P^T is done with U'' all the same
+                        readout(ring[(j - 1) % kRing], u0_prev);
+                        tc_fence_before();
+                        mbar_arrive(bar_ofree);
+                    }
                 }
                 // ---- U'' = c_t U as bf16 hi/lo (K-major A operand [d_v][t]) ----
                 if (!group_wait(bar_uo, (uint32_t)(j & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
@@ -601,7 +634,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         c[i + 3] = x.w;
                     }
                     tmem_ld32(trow + T_U + 32 * cb, v);
-                    if (cb == 0) u0 = v[0];
+                    {
+                        float w[32];
+                        tmem_ld32(trow + TW + 32 * cb, w);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += w[i];
+                    }
+                    if (cb == 0) {
+                        u0 = v[0];
+                        if (PRE_T) reinterpret_cast<float*>(smem + OFF_U0)[(j & 1) * 128 + row] = u0;
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= c[i];
                     st_split32(smem + OFF_UH, smem + OFF_UL, row, 32 * cb, v);
@@ -616,7 +658,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 if (fold && last) fold_state(R);   // otherwise folded in the next split
                 u0_prev = u0;
                 if (last) {
-                    if (rd) {
+                    if (rd && !PRE_T) {
                         if (!group_wait(bar_o, (uint32_t)(j & 1), tid == 0, BAR_CHAIN, NCHAIN, abort_flag, limit)) break;
                         tc_fence_after();
                         readout(R, u0_prev);
@@ -779,109 +821,154 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         bool staged = stage_kq(0);
 
         if constexpr (PRE_T) {
-            // T of every chunk was computed by the first passes: the group converts it and serves the
-            // chain as before (P, -sigma_0 W, padded tiles)
+            // T of every chunk was computed by the first passes: the group converts it, serves the chain as
+            // before (P, -sigma_0 W, padded tiles) and reads O out.
+            // o of chunk jj: rows 32 lq .. + 31 of this warp's lane quarter, tokens 32 half .. + 31, through a
+            // [tokens][32 rows] tile of 1 KB so that whole 16-byte pieces leave (scalar stores if o is unaligned)
+            auto read_o = [&](int jj) {
+                const Ring& Ro = ring[jj % kRing];
+                const int n = Ro.n, t0 = 32 * half;
+                if (t0 >= n) return;
+                float v[32], rs[32];
+                tmem_ld32(trow + TO + t0, v);
+                const bool single = Ro.single != 0;
+                const float qk0 = Ro.qk0;
+                const size_t tstride = (size_t)H * D;
+                const bool vec = p.o_vec16 != 0;
+                OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)(o_row0 + Ro.begin + t0) * tstride + (size_t)h * D +
+                           (vec ? 32 * lq : row);
+                OutT* stg = reinterpret_cast<OutT*>(smem + OFF_OST + pw * 1024);
+                constexpr int kTok = 1024 / (32 * (int)sizeof(OutT));   // tokens per tile: 16 bf16, 8 fp32
+                constexpr int kSeg = 32 * (int)sizeof(OutT) / 16;        // 16-byte pieces per token
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(&Ro.rs[t0 + i]);
+                    rs[i] = x.x;
+                    rs[i + 1] = x.y;
+                    rs[i + 2] = x.z;
+                    rs[i + 3] = x.w;
+                }
+                if (t0 == 0 && single)
+                    v[0] = fmaf(qk0, reinterpret_cast<const float*>(smem + OFF_U0)[(jj & 1) * 128 + row], rs[0] * v[0]);
+                else
+                    v[0] *= rs[0];
+#pragma unroll
+                for (int i = 1; i < 32; ++i) v[i] *= rs[i];
+                const int m = n - t0;
+                if (vec) {
+#pragma unroll
+                    for (int ps = 0; ps < 32 / kTok; ++ps) {
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < kTok; ++i) {
+                            if constexpr (OUT_BF16)
+                                stg[i * 32 + lane] = __float2bfloat16_rn(v[ps * kTok + i]);
+                            else
+                                stg[i * 32 + lane] = v[ps * kTok + i];
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < kTok * kSeg / 32; ++k) {
+                            const int e = 32 * k + lane, i = e / kSeg, u = e % kSeg;
+                            const int t = ps * kTok + i;
+                            if (t < m)
+                                *reinterpret_cast<uint4*>(ob + (size_t)t * tstride + u * (16 / sizeof(OutT))) =
+                                    *reinterpret_cast<const uint4*>(stg + i * 32 + u * (16 / sizeof(OutT)));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if (i < m) {
+                            if constexpr (OUT_BF16)
+                                ob[(size_t)i * tstride] = __float2bfloat16_rn(v[i]);
+                            else
+                                ob[(size_t)i * tstride] = v[i];
+                        }
+                    }
+                }
+            };
             for (int j = 0; staged; ++j) {
                 const Ring& R = ring[j % kRing];
                 const int n = R.n;
                 const bool single = R.single != 0;
                 const bool last = R.last != 0;
-                const float* ps = psc + (j & 1) * 4 * C;
-                if (pw == 3 && !last) compute_chunk(j + 1);   // the gate warp runs one chunk ahead
 
-                // ---- this chunk's V (rows past the chunk zeroed) ----
+                // ---- this chunk's V and T operand tiles; rows past the chunk (later tokens) zeroed ----
                 if (!group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                if (!group_wait(bar_t, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
                 if (n < C) {
                     const int nz = C - n;
-                    for (int i = ptid; i < 2 * nz * 8; i += NPREP) {
+                    for (int i = ptid; i < 6 * nz * 8; i += NPREP) {   // V: two column blocks; T: four planes
                         const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;
-                        *reinterpret_cast<uint4*>(smem + OFF_V + part * 8192 + (n + rz) * 128 + seg * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                        unsigned char* base = part < 2 ? smem + OFF_V + part * 8192 : smem + OFF_T1H + (part - 2) * 8192;
+                        *reinterpret_cast<uint4*>(base + (n + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
+                    proxy_fence();
                 }
-                // ---- T -> T diag(beta gamma), T diag(beta) as bf16 hi/lo K-major operands; rows past the
-                //      chunk (later tokens' T rows) become zero ----
-                if (!group_wait(bar_t, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
-                {
-                    const float* Tt = reinterpret_cast<const float*>(smem + OFF_LF);
-                    const float* sg_bg = ps + 2 * C;
-                    const float* sg_b = ps + 3 * C;
-                    const int t = ptid >> 2, c0 = 16 * (ptid & 3);
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int cc = c0 + 8 * q;
-                        uint32_t h1[4] = {0u, 0u, 0u, 0u}, l1[4] = {0u, 0u, 0u, 0u};
-                        uint32_t h2[4] = {0u, 0u, 0u, 0u}, l2[4] = {0u, 0u, 0u, 0u};
-                        if (t < n) {
-                            const float4 x0 = *reinterpret_cast<const float4*>(Tt + t * C + cc);
-                            const float4 x1 = *reinterpret_cast<const float4*>(Tt + t * C + cc + 4);
-                            const float4 a0 = *reinterpret_cast<const float4*>(sg_bg + cc);
-                            const float4 a1 = *reinterpret_cast<const float4*>(sg_bg + cc + 4);
-                            const float4 b0 = *reinterpret_cast<const float4*>(sg_b + cc);
-                            const float4 b1 = *reinterpret_cast<const float4*>(sg_b + cc + 4);
-                            split_pair(x0.x * a0.x, x0.y * a0.y, h1[0], l1[0]);
-                            split_pair(x0.z * a0.z, x0.w * a0.w, h1[1], l1[1]);
-                            split_pair(x1.x * a1.x, x1.y * a1.y, h1[2], l1[2]);
-                            split_pair(x1.z * a1.z, x1.w * a1.w, h1[3], l1[3]);
-                            split_pair(x0.x * b0.x, x0.y * b0.y, h2[0], l2[0]);
-                            split_pair(x0.z * b0.z, x0.w * b0.w, h2[1], l2[1]);
-                            split_pair(x1.x * b1.x, x1.y * b1.y, h2[2], l2[2]);
-                            split_pair(x1.z * b1.z, x1.w * b1.w, h2[3], l2[3]);
-                        }
-                        const uint32_t o = sw128(t, cc);
-                        *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-                        *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-                        *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-                        *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
-                    }
-                }
-                proxy_fence();
                 group_sync(BAR_PREP, NPREP);
-                if (leader) {
-                    mbar_arrive(bar_wuin);
-                    if (!last && allowed(j + 1)) issue_t(j + 1, R.next_begin);   // the T area is free again
-                }
+                if (leader) mbar_arrive(bar_wuin);
+                if (pw == 3 && !last) compute_chunk(j + 1);   // the gate warp runs one chunk ahead, off the barriers
 
                 // ---- W^T = K^T T1^T, U~^T = V^T T2^T; then -sigma_0 W^T as the MN-major B operand: first, as
                 //      the chain's next U^T waits for it, while P waits for the previous readout ----
                 if (!group_wait(bar_wu, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
                 tc_fence_after();
-                if (leader && !last && allowed(j + 1)) issue_v(j + 1, R.next_begin);   // the V buffer is free again
+                if (leader && !last && allowed(j + 1)) {   // the V and T tiles are free again
+                    issue_v(j + 1, R.next_begin);
+                    issue_t(j + 1, R.next_begin);
+                }
                 {
                     const float f = -R.sigma0;
                     float v[32];
-                    tmem_ld32(trow + T_W + 32 * half, v);
+                    tmem_ld32(trow + TW + 32 * half, v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= f;
                     st_split32(smem + OFF_WH, smem + OFF_WL, row, 32 * half, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    tmem_st32(trow + TW + 32 * half, v);   // U^T's second half accumulates from zero
+                    tmem_st_wait();
                 }
                 proxy_fence();
                 tc_fence_before();
                 mbar_arrive(bar_wready);
 
-                // ---- P = mask(q_t . k_s) from the Q rows of [K; Q] K^T, once the chain's previous U''^T P^T is
-                //      done; then the next chunk's K/Q tiles ----
+                // ---- once the chain's previous U''^T P^T is done: read O of the previous chunk out, then P =
+                //      mask(q_t . k_s) from the Q rows of [K; Q] K^T; then the next chunk's K/Q tiles ----
                 if (rd) {
-                    if (j > 0 && !group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
-                        break;
+                    if (j > 0) {
+                        if (!group_wait(bar_o, (uint32_t)((j - 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+                        tc_fence_after();
+                        read_o(j - 1);
+                        tc_fence_before();
+                        mbar_arrive(bar_ofree);
+                    }
                     if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
                     tc_fence_after();
                     if (lq >= 2) {
                         float v[32];
-                        tmem_ld32(trow + T_G + 32 * half, v);
+                        tmem_ld32(trow + TG + 32 * half, v);
                         const int t = row - 64, s0 = 32 * half;
                         if (single && t == 0 && half == 0) ring[j % kRing].qk0 = v[0];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = (!single && s0 + i <= t) ? v[i] : 0.f;
                         st_split32(smem + OFF_PH, smem + OFF_PL, t, s0, v);
                     }
-                    proxy_fence();
                     tc_fence_before();
+                    proxy_fence();
                     mbar_arrive(bar_pready);
                 }
                 if (!last && !(staged = stage_kq(j + 1))) break;
 
-                if (last) break;
+                if (last) {
+                    // the last chunk's O
+                    if (rd && group_wait(bar_o, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) {
+                        tc_fence_after();
+                        read_o(j);
+                    }
+                    break;
+                }
             }
         } else {
         for (int j = 0; staged; ++j) {
@@ -904,7 +991,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             }
             if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             tc_fence_after();
-            const int g8 = lane >> 2, t4 = lane & 3;
             // ---- L (fp32, zero on and above the diagonal) from the K rows of [K; Q] K^T; diagonal blocks to Ld ----
             if (lq < 2) {
                 const int t = row, s0 = 32 * half;
@@ -919,7 +1005,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 }
                 const float f = ps[2 * C + t];
                 float v[32];
-                tmem_ld32(trow + T_G + 32 * half, v);
+                tmem_ld32(trow + TG + 32 * half, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = (s0 + i < t) ? f * gi[i] * v[i] : 0.f;
 #pragma unroll
@@ -949,7 +1035,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 4 (rows 0-31 of G, columns
             //      0-31) and warp 9 (rows 32-63, columns 32-63) each take a whole diagonal 32-block of L and
             //      invert it alone: two 16x16 forward substitutions and one merge, then its T operands;
-            //      the gate warp runs a chunk ahead. ----
+            //      the gate warp runs a chunk ahead.  The merge within a diagonal block runs in fp32 on the
+            //      CUDA cores; the lower-left block on mma.sync tf32 (hi/lo split) over all prep warps. ----
             if (pw == 0 || pw == 5) {
                 const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant: rows / columns 32 qw .. + 31
                 const int t = row, s0 = 32 * half;         // warp 4: t 0-31, s 0-31; warp 9: t 32-63, s 32-63
@@ -971,50 +1058,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         for (int r = 0; r < 16; ++r) Lf[(16 * bb + r) * kLdF + 16 * bb + jc] = x[r];
                     }
                     __syncwarp();
-                    // merge: T_ib,jb = -T_ib,ib (L_ib,jb T_jb,jb), (jb, ib) = (2 qw, 2 qw + 1), on mma.sync tf32
+                    // merge: T_ib,jb = -T_ib,ib (L_ib,jb T_jb,jb), (jb, ib) = (2 qw, 2 qw + 1), in fp32 on the CUDA
+                    // cores (the tensor pipe is busy with the chain's products): lane = column c, half = 8 rows
                     {
-                        const int jb = 2 * qw, ib = jb + 1;
-                        float* sc = Ld + jb * 16 * 17;   // this warp's diagonal blocks are no longer needed
-                        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                        float yc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        const int jb = 2 * qw, ib = jb + 1, c = lane & 15, rh = lane >> 4;
+                        const float* Lij = Lf + (16 * ib) * kLdF + 16 * jb;
+                        const float* Tjj = Lf + (16 * jb) * kLdF + 16 * jb;
+                        const float* Tii = Lf + (16 * ib) * kLdF + 16 * ib;
+                        float y[8];
 #pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
+                        for (int r = 0; r < 8; ++r) y[r] = 0.f;
 #pragma unroll
-                            for (int ks = 0; ks < 2; ++ks)
-                                mma_tf32x3(y[nt], yc[nt], Lf + (16 * ib) * kLdF + 16 * jb + 8 * ks, kLdF,
-                                           Lf + (16 * jb + 8 * ks) * kLdF + 16 * jb + 8 * nt, kLdF, g8, t4);
+                        for (int k = 0; k < 16; ++k) {
+                            const float tk = Tjj[k * kLdF + c];
 #pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) y[nt][e] += yc[nt][e];
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            sc[g8 * 16 + 8 * nt + 2 * t4] = y[nt][0];
-                            sc[g8 * 16 + 8 * nt + 2 * t4 + 1] = y[nt][1];
-                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4] = y[nt][2];
-                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4 + 1] = y[nt][3];
+                            for (int r = 0; r < 8; ++r) y[r] = fmaf(Lij[(8 * rh + r) * kLdF + k], tk, y[r]);
                         }
-                        __syncwarp();
-                        float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                        float xc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                        float ylo[8], yhi[8];   // column c of L_ib,jb T_jb,jb, rows 0-7 and 8-15
 #pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int ks = 0; ks < 2; ++ks)
-                                mma_tf32x3(x[nt], xc[nt], Lf + (16 * ib) * kLdF + 16 * ib + 8 * ks, kLdF,
-                                           sc + 8 * ks * 16 + 8 * nt, 16, g8, t4);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) x[nt][e] += xc[nt][e];
-                        float* dst = Lf + (16 * ib) * kLdF + 16 * jb;
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            dst[g8 * kLdF + 8 * nt + 2 * t4] = -x[nt][0];
-                            dst[g8 * kLdF + 8 * nt + 2 * t4 + 1] = -x[nt][1];
-                            dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4] = -x[nt][2];
-                            dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4 + 1] = -x[nt][3];
+                        for (int r = 0; r < 8; ++r) {
+                            const float o = __shfl_xor_sync(0xffffffffu, y[r], 16);
+                            ylo[r] = rh ? o : y[r];
+                            yhi[r] = rh ? y[r] : o;
                         }
+                        float x[8];
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) x[r] = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const float yk = k < 8 ? ylo[k] : yhi[k - 8];
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) x[r] = fmaf(Tii[(8 * rh + r) * kLdF + k], yk, x[r]);
+                        }
+                        __syncwarp();   // every lane is done with L_ib,jb
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) Lf[(16 * ib + 8 * rh + r) * kLdF + 16 * jb + c] = -x[r];
                     }
                     __syncwarp();
                     // this 32-block's T operands: row t, columns s0 .. s0 + 31, 8 columns per 16-byte store
@@ -1047,6 +1125,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             }
             group_sync(BAR_PREP, NPREP);
             {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block on mma.sync tf32; warp = (row, column) tile
+                const int g8 = lane >> 2, t4 = lane & 3;
                 const int mt = pw >> 2, nt = pw & 3;
                 float y[4] = {0.f, 0.f, 0.f, 0.f}, yc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1083,7 +1162,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 tc_fence_after();
                 if (lq >= 2) {
                     float v[32];
-                    tmem_ld32(trow + T_G + 32 * half, v);
+                    tmem_ld32(trow + TG + 32 * half, v);
                     const int t = row - 64, s0 = 32 * half;
                     if (single && t == 0 && half == 0) ring[j % kRing].qk0 = v[0];
 #pragma unroll
@@ -1104,10 +1183,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             {
                 const float f = -R.sigma0;
                 float v[32];
-                tmem_ld32(trow + T_W + 32 * half, v);
+                tmem_ld32(trow + TW + 32 * half, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= f;
                 st_split32(smem + OFF_WH, smem + OFF_WL, row, 32 * half, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                tmem_st32(trow + TW + 32 * half, v);   // U^T's second half accumulates from zero
+                tmem_st_wait();
             }
             proxy_fence();
             tc_fence_before();
@@ -1133,12 +1216,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
                 if (sp == 0 && mbar_test(bar_gin, jp & 1)) {
                     tc_fence_after();
-                    // [K; Q] K^T: its K rows give L, its Q rows P (with T given, only P is needed)
+                    // [K; Q] K^T: its K rows give L, its Q rows P (with T given only P, and only with a readout)
                     if (!PRE_T || rd) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            umma_ss(tbase + T_G, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64,
+                            umma_ss(tbase + TG, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64,
                                     kk > 0);
                         }
                         umma_commit(bar_g);
@@ -1155,8 +1238,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
                         const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
-                        umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
-                        umma_ss(tbase + T_W, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
+                        umma_ss(tbase + TW, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
+                        umma_ss(tbase + TW, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
                         umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
                         umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
                     }
@@ -1182,10 +1265,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t bwh = sdesc(sbase + OFF_WH + kk * 2048, 16384, 1024);
-                            const uint64_t bwl = sdesc(sbase + OFF_WL + kk * 2048, 16384, 1024);
                             const uint32_t ah = tbase + T_SH + 8 * kk, al = tbase + T_SL + 8 * kk;
-                            umma_ts(tbase + T_U, ah, bwh, id64b, 1);
-                            umma_ts(tbase + T_U, ah, bwl, id64b, 1);
+                            // [U | W] += S_hi [W_hi | W_lo]^T (N = 128: W_lo follows W_hi at the block stride)
+                            umma_ts(tbase + T_U, ah, bwh, id128b, 1);
                             umma_ts(tbase + T_U, al, bwh, id64b, 1);
                         }
                         umma_commit(bar_uo);
@@ -1201,8 +1283,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t bq = sdesc(inKQ + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                            umma_ts(tbase + T_O, tbase + T_SH + 8 * kk, bq, id64, kk > 0);
-                            umma_ts(tbase + T_O, tbase + T_SL + 8 * kk, bq, id64, 1);
+                            umma_ts(tbase + TO, tbase + T_SH + 8 * kk, bq, id64, kk > 0);
+                            umma_ts(tbase + TO, tbase + T_SL + 8 * kk, bq, id64, 1);
                         }
                         sc = 2;
                         progressed = true;
@@ -1237,9 +1319,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                                 const uint64_t aul = sdesc(sbase + OFF_UL + kt * 32, 16, 1024);
                                 const uint64_t bph = sdesc(sbase + OFF_PH + kt * 32, 16, 1024);
                                 const uint64_t bpl = sdesc(sbase + OFF_PL + kt * 32, 16, 1024);
-                                umma_ss(tbase + T_O, auh, bph, id64, 1);
-                                umma_ss(tbase + T_O, auh, bpl, id64, 1);
-                                umma_ss(tbase + T_O, aul, bph, id64, 1);
+                                umma_ss(tbase + TO, auh, bph, id64, 1);
+                                umma_ss(tbase + TO, auh, bpl, id64, 1);
+                                umma_ss(tbase + TO, aul, bph, id64, 1);
                             }
                         }
                         umma_commit(bar_o);
@@ -1301,7 +1383,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 template <bool OUT_BF16, bool READOUT, bool PRE_T>
 cudaError_t launch_chunk_tc(const Params& p, int grid, cudaStream_t stream) {
     auto kern = gdn_chunk_tc_kernel<OUT_BF16, READOUT, PRE_T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static std::atomic<int> optin[kMaxOptinDevices];
+    cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), kSmemBytes, optin);
     if (e != cudaSuccess) return e;
     kern<<<grid, NTHREADS, kSmemBytes, stream>>>(p);
     return cudaGetLastError();

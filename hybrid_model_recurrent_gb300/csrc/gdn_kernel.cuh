@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <type_traits>
 
 namespace gdn {
@@ -94,10 +95,13 @@ struct Params {
     int32_t o_vec16;        // o is 16-byte aligned: the chunked kernel may write it in 16-byte pieces
     // two-pass chunked path only: the chunk schedule and T = (I + L)^-1 of every chunk, computed by
     // parallel passes before the state scan (workspace buffers)
-    CUtensorMap tm_t;       // t_rows as [rows, 64] fp32, box (64, 64)
+    CUtensorMap tm_t;       // t_ops as [4 * t_rows, 64] bf16, box (64, 64), 128-byte swizzle
     int32_t* chunk_beg;     // [rows]: chunk c of (job, head) starts at token chunk_beg[t_row0 + head * len + c]
     int32_t* chunk_cnt;     // [n_jobs, H]: chunks of (job, head)
-    float* t_rows;          // [rows, 64]: row t_row0 + head * len + t is row t - begin of its chunk's T
+    void* t_ops;            // bf16 [4][t_rows][64]: T diag(beta gamma) hi, lo, T diag(beta) hi, lo; row
+                            // t_row0 + head * len + t holds row t - begin of its chunk
+    int32_t t_rows;         // rows of each of the four planes
+    int32_t pad2_;
     Job jobs[kMaxJobs];
     Ckpt ckpts[kMaxCkpts];
 };
@@ -593,11 +597,30 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     }
 }
 
+// The dynamic shared-memory opt-in of a kernel, made once per device (again only for a larger size): the
+// attribute call costs host time, and a short kernel's successor must not wait for it on the device.
+constexpr int kMaxOptinDevices = 64;
+inline cudaError_t smem_optin(const void* kern, int bytes, std::atomic<int>* done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool track = dev >= 0 && dev < kMaxOptinDevices;
+    if (track && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && track) {
+        int cur = done[dev].load();
+        while (cur < bytes && !done[dev].compare_exchange_weak(cur, bytes)) {
+        }
+    }
+    return e;
+}
+
 // Launch one kernel instance; instantiated per d_k in inst_dk*.cu.
 template <int DK, bool IN_BF16, bool OUT_BF16, bool READOUT, bool TWIN>
 cudaError_t launch_scan(const Params& p, int grid, size_t smem, cudaStream_t stream) {
     auto kern = gdn_scan_kernel<DK, IN_BF16, OUT_BF16, READOUT, TWIN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<int> optin[kMaxOptinDevices];
+    cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), (int)smem, optin);
     if (e != cudaSuccess) return e;
     kern<<<grid, 32 * (p.nw + 1), smem, stream>>>(p);
     return cudaGetLastError();

@@ -8,8 +8,9 @@
 //   schedule_kernel - the chunk starts of each (job, head): windows of 64 tokens from the previous
 //       chunk end, cut at the next checkpoint and before the token where gamma falls below 2^-32
 //       (the rule the scan kernel's gate warp applies, with the same rounding);
-//   tprep_kernel    - T of every chunk in fp32 (tf32 x 3 merges on mma.sync, K K^T on bf16 mma.sync),
-//       stored as rows indexed by token, so the storage is bounded by the tokens scanned.
+//   tprep_kernel    - T of every chunk in fp32 (tf32 x 3 merges on mma.sync, K K^T on bf16 mma.sync), stored
+//       as the scan's MMA operands T diag(beta gamma) and T diag(beta), each split into bf16 hi + lo, in rows
+//       indexed by token, so the storage is bounded by the tokens scanned.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -77,37 +78,24 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
     if (threadIdx.x == 0) p.chunk_cnt[s] = cnt;
 }
 
-// ---- T of every chunk: 4 warps per chunk, K double buffered by TMA ----
+// ---- T of every chunk: 4 warps per chunk; the next chunk's K is copied in once K K^T is done, and its
+//      gates are loaded a chunk ahead ----
 constexpr int kTpThreads = 128;
+constexpr int kTpBlocksPerSm = 5;
 constexpr int kTpLd = 68;                    // fp32 elements per row of L / T in shared memory
-constexpr int TP_K = 0;                      // 2 x 16 KB: K as two 64-column blocks of [64 rows][128 B], swizzled
-constexpr int TP_L = 32768;                  // fp32 [64][68]: L, then T in place
+constexpr int TP_K = 0;                      // 16 KB: K as two 64-column blocks of [64 rows][128 B], swizzled
+constexpr int TP_L = 16384;                  // fp32 [64][68]: L, then T in place
 constexpr int TP_Y = TP_L + C * kTpLd * 4;   // fp32 [32][33] scratch of the merges
-constexpr int TP_G = TP_Y + 32 * 33 * 4;     // fp32 [2][64]: beta gamma, 1/gamma
-constexpr int TP_BAR = TP_G + 2 * C * 4;     // 2 mbarriers
+constexpr int TP_G = TP_Y + 32 * 33 * 4;     // fp32 [3][64]: beta gamma, 1/gamma, beta
+constexpr int TP_BAR = TP_G + 3 * C * 4;     // 1 mbarrier
 constexpr int kTpSmemBytes = TP_BAR + 64 + 1024;
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 // shared-memory address of K element (row, col), col % 8 == 0, in a swizzled buffer at kbase
 __device__ __forceinline__ uint32_t k_addr(uint32_t kbase, int row, int col) {
     return kbase + (uint32_t)((col >> 6) * 8192) + sw128(row, col & 63);
 }
 
-__global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kTpThreads, kTpBlocksPerSm) tprep_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char tp_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tp_raw) + 1023u) & ~uintptr_t(1023));
@@ -115,6 +103,7 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
     float* sy = reinterpret_cast<float*>(smem + TP_Y);
     float* sbg = reinterpret_cast<float*>(smem + TP_G);
     float* sgi = sbg + C;
+    float* sbe = sbg + 2 * C;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + TP_BAR);
     const uint32_t kbase0 = smem_addr(smem + TP_K);
 
@@ -124,7 +113,9 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
     const int len = job.len;
     const int nch = p.chunk_cnt[s];
     const int32_t* beg = p.chunk_beg + (size_t)job.t_row0 + (size_t)h * (size_t)len;
-    float* tout = p.t_rows + ((size_t)job.t_row0 + (size_t)h * (size_t)len) * C;
+    const size_t trow0 = (size_t)job.t_row0 + (size_t)h * (size_t)len;
+    const size_t plane = (size_t)p.t_rows * C;
+    __nv_bfloat16* tout = reinterpret_cast<__nv_bfloat16*>(p.t_ops) + trow0 * C;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
     const uint64_t limit = p.wait_limit_ns;
@@ -133,7 +124,6 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
         fence_barrier_init();
     }
     // the blocks above the diagonal of L and T are never written: zero them once
@@ -143,48 +133,58 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
     }
     __syncthreads();
 
-    int issued0 = 0, issued1 = 0;   // thread 0: copies issued into each buffer
-    auto issue_k = [&](int c, int buf) {
+    int issued = 0;   // thread 0: copies issued
+    auto issue_k = [&](int c) {
         const int t0 = (int)(job.tok_begin + beg[c]);
-        unsigned char* dst = smem + TP_K + buf * 16384;
+        unsigned char* dst = smem + TP_K;
         proxy_fence();
-        mbar_arrive_expect_tx(&bar[buf], 16384u);
-        tma_load_3d(dst, &p.tm_k, 0, h, t0, &bar[buf]);
-        tma_load_3d(dst + 8192, &p.tm_k, 64, h, t0, &bar[buf]);
-        if (buf) ++issued1; else ++issued0;
+        mbar_arrive_expect_tx(&bar[0], 16384u);
+        tma_load_3d(dst, &p.tm_k, 0, h, t0, &bar[0]);
+        tma_load_3d(dst + 8192, &p.tm_k, 64, h, t0, &bar[0]);
+        ++issued;
     };
-    if (tid == 0) issue_k(blockIdx.x, 0);
+    // warp 0: alpha, beta of a chunk (1 and 0 past its end), held in registers a chunk ahead
+    float ga0 = 1.f, ga1 = 1.f, gb0 = 0.f, gb1 = 0.f;
+    auto load_gates = [&](int c) {
+        const int bc = beg[c];
+        const int nc = (c + 1 < nch ? beg[c + 1] : len) - bc;
+        const size_t g = (size_t)(job.tok_begin + bc) * (size_t)H + (size_t)h;
+        ga0 = lane < nc ? __ldg(p.alpha + g + (size_t)lane * H) : 1.f;
+        ga1 = lane + 32 < nc ? __ldg(p.alpha + g + (size_t)(lane + 32) * H) : 1.f;
+        gb0 = lane < nc ? __ldg(p.beta + g + (size_t)lane * H) : 0.f;
+        gb1 = lane + 32 < nc ? __ldg(p.beta + g + (size_t)(lane + 32) * H) : 0.f;
+    };
+    if (tid == 0) issue_k(blockIdx.x);
+    if (warp == 0) load_gates(blockIdx.x);
 
     bool ok = true;
     for (int i = 0;; ++i) {
         const int c = blockIdx.x + i * gridDim.x;
         if (c >= nch) break;
-        const int buf = i & 1;
         const int b = beg[c];
         const int n = (c + 1 < nch ? beg[c + 1] : len) - b;
-        if (tid == 0 && c + (int)gridDim.x < nch) issue_k(c + gridDim.x, buf ^ 1);
-        // gates of the chunk: gamma (the scan's rounding), beta gamma and 1/gamma
+        const bool more = c + (int)gridDim.x < nch;
+        // gates of the chunk: gamma (the scan's rounding), beta gamma and 1/gamma; then the next chunk's
         if (warp == 0) {
-            const size_t g = (size_t)(job.tok_begin + b) * (size_t)H + (size_t)h;
-            const float a0 = lane < n ? __ldg(p.alpha + g + (size_t)lane * H) : 1.f;
-            const float a1 = lane + 32 < n ? __ldg(p.alpha + g + (size_t)(lane + 32) * H) : 1.f;
-            const float b0 = lane < n ? __ldg(p.beta + g + (size_t)lane * H) : 0.f;
-            const float b1 = lane + 32 < n ? __ldg(p.beta + g + (size_t)(lane + 32) * H) : 0.f;
+            const float a0 = ga0, a1 = ga1, b0 = gb0, b1 = gb1;
+            if (more) load_gates(c + gridDim.x);
             float g0, g1;
             gate_prefix(a0, a1, g0, g1, lane);
             sbg[lane] = b0 * g0;
             sbg[lane + 32] = b1 * g1;
             sgi[lane] = __frcp_rn(g0);
             sgi[lane + 32] = __frcp_rn(g1);
+            sbe[lane] = b0;
+            sbe[lane + 32] = b1;
         }
         // this chunk's K (bounded wait by one poller; then every thread observes the phase itself)
         {
             bool got = true;
             if (tid == 0) {
-                const uint32_t par = (uint32_t)((i >> 1) & 1);
-                if (!mbar_try_wait(&bar[buf], par)) {
+                const uint32_t par = (uint32_t)(i & 1);
+                if (!mbar_try_wait(&bar[0], par)) {
                     const uint64_t t0 = global_ns();
-                    while (!(got = mbar_try_wait(&bar[buf], par)))
+                    while (!(got = mbar_try_wait(&bar[0], par)))
                         if (global_ns() - t0 > limit) break;
                 }
             }
@@ -192,10 +192,10 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
                 ok = false;
                 break;
             }
-            mbar_try_wait(&bar[buf], (uint32_t)((i >> 1) & 1));
+            mbar_try_wait(&bar[0], (uint32_t)(i & 1));
         }
-        const uint32_t kb = kbase0 + (uint32_t)(buf * 16384);
-        unsigned char* kp = smem + TP_K + buf * 16384;
+        const uint32_t kb = kbase0;
+        unsigned char* kp = smem + TP_K;
         if (n < C) {   // rows past the chunk belong to later tokens: zero them
             const int nz = C - n;
             for (int e = tid; e < 2 * nz * 8; e += kTpThreads) {
@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
             }
         }
         __syncthreads();
+        if (tid == 0 && more) issue_k(c + gridDim.x);   // K K^T is done: the buffer takes the next chunk's K
         // ---- the four 16x16 diagonal blocks of T by forward substitution: warp w, block w, lane = column ----
         {
             const int jc = lane & 15;
@@ -334,18 +335,31 @@ __global__ void __launch_bounds__(kTpThreads, 4) tprep_kernel(const __grid_const
             }
         }
         __syncthreads();
-        // ---- rows 0 .. n-1 of T to their tokens' rows ----
-        for (int e = tid; e < n * 16; e += kTpThreads) {
-            const int r = e >> 4, q = e & 15;
-            *reinterpret_cast<float4*>(tout + (size_t)(b + r) * C + 4 * q) =
-                *reinterpret_cast<const float4*>(sl + r * kTpLd + 4 * q);
+        // ---- rows 0 .. n-1 of T diag(beta gamma) and T diag(beta), split x = hi + lo into bf16, to their
+        //      tokens' rows of the four planes; 8 columns per item ----
+        for (int e = tid; e < n * 8; e += kTpThreads) {
+            const int r = e >> 3, c0 = 8 * (e & 7);
+            const float4 x0 = *reinterpret_cast<const float4*>(sl + r * kTpLd + c0);
+            const float4 x1 = *reinterpret_cast<const float4*>(sl + r * kTpLd + c0 + 4);
+            const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int s0 = c0 + 2 * q;
+                split_pair(x[2 * q] * sbg[s0], x[2 * q + 1] * sbg[s0 + 1], h1[q], l1[q]);
+                split_pair(x[2 * q] * sbe[s0], x[2 * q + 1] * sbe[s0 + 1], h2[q], l2[q]);
+            }
+            __nv_bfloat16* dst = tout + (size_t)(b + r) * C + c0;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+            *reinterpret_cast<uint4*>(dst + plane) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+            *reinterpret_cast<uint4*>(dst + 2 * plane) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(dst + 3 * plane) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
         }
         __syncthreads();   // T and the K buffer are free for the next chunk
     }
     if (!ok && tid == 0) {
-        // a copy may still be in flight into either buffer: wait for it (bounded) before leaving
-        if (issued0 > 0) drain_phase(&bar[0], (uint32_t)((issued0 - 1) & 1), drain_limit);
-        if (issued1 > 0) drain_phase(&bar[1], (uint32_t)((issued1 - 1) & 1), drain_limit);
+        // a copy may still be in flight into the buffer: wait for it (bounded) before leaving
+        if (issued > 0) drain_phase(&bar[0], (uint32_t)((issued - 1) & 1), drain_limit);
         atomicOr(p.status, STATUS_TIMEOUT);
     }
 }
@@ -360,16 +374,23 @@ cudaError_t launch_schedule(const Params& p, int n_streams, cudaStream_t stream)
 
 cudaError_t launch_tprep(const Params& p, int n_streams, cudaStream_t stream) {
     if (n_streams <= 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(tprep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTpSmemBytes);
+    static std::atomic<int> optin[kMaxOptinDevices];
+    static std::atomic<int> slots_of[kMaxOptinDevices];   // resident blocks on the whole device, once known
+    cudaError_t e = smem_optin(reinterpret_cast<const void*>(tprep_kernel), kTpSmemBytes, optin);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tprep_kernel, kTpThreads, kTpSmemBytes)) !=
-        cudaSuccess)
-        return e;
+    int slots = (dev >= 0 && dev < kMaxOptinDevices) ? slots_of[dev].load() : 0;
+    if (slots <= 0) {
+        int sms = 0, per_sm = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tprep_kernel, kTpThreads, kTpSmemBytes)) !=
+            cudaSuccess)
+            return e;
+        slots = sms * (per_sm > 0 ? per_sm : 1);
+        if (dev >= 0 && dev < kMaxOptinDevices) slots_of[dev].store(slots);
+    }
     // one wave: the chunks of a (job, head) are dealt round robin to its blocks
-    const int slots = sms * (per_sm > 0 ? per_sm : 1);
     const int per_stream = slots / n_streams > 1 ? slots / n_streams : 1;
     const dim3 grid((unsigned)per_stream, (unsigned)n_streams);
     tprep_kernel<<<grid, kTpThreads, kTpSmemBytes, stream>>>(p);

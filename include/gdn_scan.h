@@ -375,8 +375,9 @@ size_t gdn_workspace_size(void);
  * resume: the sum of the probe depths bounds it; tail replay: the sum of the
  * tails, plus the sum of m when S_a is given), `num_ranges` = ranges scanned
  * (sequences, probes; twice the sequences for a replay with S_a).  It holds
- * the status word, the chunk schedule and T = (I + L)^-1 (64 fp32 per token
- * and head).  0 for negative arguments or more than 2^31 token-heads. */
+ * the status word, the chunk schedule and the T = (I + L)^-1 operands (256
+ * bf16 per token and head).  0 for negative arguments or 2^29 - 64 token-heads
+ * or more. */
 size_t gdn_workspace_size_two_pass(int64_t tokens, int32_t num_heads, int32_t num_ranges);
 
 /* Zero the sticky status word of a workspace (enqueued on stream). */

@@ -147,16 +147,17 @@ def test_two_pass_workspace_size(L):
     base = L.gdn_workspace_size()
     f = L.gdn_workspace_size_two_pass
     assert f(0, 1, 0) == base
-    # status word, chunk counts (4 B per range and head), chunk starts (4 B per token and head), T rows
-    # (64 fp32 per token and head), each part 256-byte aligned
+    # status word, chunk counts (4 B per range and head), chunk starts (4 B per token and head), T operand
+    # rows (4 planes x 64 bf16 per token and head), each part 256-byte aligned
     up = lambda x: (x + 255) // 256 * 256
     for T, H, R in ((30, 2, 2), (8192 * 8, 16, 8), (1, 1, 1), (1000, 3, 7)):
         cnt = base
         beg = up(cnt + 4 * R * H)
         t = up(beg + 4 * T * H)
-        assert f(T, H, R) == t + 256 * T * H
+        assert f(T, H, R) == t + 512 * T * H
     assert f(-1, 1, 1) == 0 and f(1, 0, 1) == 0 and f(1, 1, -1) == 0
-    assert f(1 << 31, 1, 1) == 0 and f(1 << 27, 16, 1) == 0     # more than 2^31 - 1 token-heads
+    assert f(1 << 29, 1, 1) == 0 and f(1 << 25, 16, 1) == 0     # 2^29 - 64 token-heads or more
+    assert f((1 << 29) - 65, 1, 1) > 0
 
 
 def test_resume_and_replay_reject_bad_arguments(L):
