@@ -65,7 +65,7 @@ constexpr int D = 128;
 constexpr int NCHAIN = 128;                  // warps 0-3
 constexpr int NPREP = 256;                   // warps 4-11
 constexpr int NTHREADS = NCHAIN + NPREP + 32;   // + warp 12: MMA issue
-constexpr int BAR_CHAIN = 1, BAR_PREP = 2, BAR_PREP_A = 3;   // named barriers (3 and 4: halves of prep)
+constexpr int BAR_CHAIN = 1, BAR_PREP = 2;   // named barriers
 constexpr int kRing = 4;                     // chunk schedule entries in flight
 
 struct Pos {   // chunk schedule cursor
@@ -978,17 +978,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             const bool last = R.last != 0;
             const float* ps = psc + (j & 1) * 4 * C;
 
-            // ---- this chunk's V (rows past the chunk zeroed); its [K; Q] K^T was issued a chunk ago ----
-            if (!group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
-            if (n < C) {
-                const int nz = C - n;
-                for (int i = ptid; i < 2 * nz * 8; i += NPREP) {
-                    const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;
-                    *reinterpret_cast<uint4*>(smem + OFF_V + part * 8192 + (n + rz) * 128 + seg * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                proxy_fence();
-            }
+            // ---- this chunk's [K; Q] K^T, issued a chunk ago ----
             if (!group_wait(bar_g, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             tc_fence_after();
             // ---- L (fp32, zero on and above the diagonal) from the K rows of [K; Q] K^T; diagonal blocks to Ld ----
@@ -1149,6 +1139,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 for (int e = 0; e < 4; ++e) x[e] += xc[e];
                 put_t12(32 + 16 * mt + g8, 8 * nt + 2 * t4, -x[0], -x[1]);
                 put_t12(32 + 16 * mt + g8 + 8, 8 * nt + 2 * t4, -x[2], -x[3]);
+            }
+            // ---- this chunk's V (rows past the chunk zeroed): landed while T was formed ----
+            if (!group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
+            if (n < C) {
+                const int nz = C - n;
+                for (int i = ptid; i < 2 * nz * 8; i += NPREP) {
+                    const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;
+                    *reinterpret_cast<uint4*>(smem + OFF_V + part * 8192 + (n + rz) * 128 + seg * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             proxy_fence();
             group_sync(BAR_PREP, NPREP);
