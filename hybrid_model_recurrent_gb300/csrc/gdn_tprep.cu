@@ -24,11 +24,16 @@ namespace {
 
 constexpr int kSchedThreads = 256;
 constexpr int kSchedTile = 8192;   // gates of one (job, head) staged per pass
+constexpr int kSchedWins = 256;    // windows judged at once
 
-// ---- chunk schedule: one block per (job, head); warp 0 walks the chunks over gates staged in shared memory ----
+// ---- chunk schedule: one block per (job, head).  The windows a walk without gamma cuts would take (64
+//      tokens from the previous end, cut at the next checkpoint) are listed first, all of them judged at once
+//      by the 8 warps with the same rule and rounding as the scan's gate warp; the walk then takes the windows
+//      in order up to the first that is cut early, and lists the windows again from its end. ----
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_constant__ Params p) {
     __shared__ float sa[kSchedTile + C];
-    __shared__ int s_pos, s_cnt;
+    __shared__ int ws[kSchedWins], wl[kSchedWins], wn[kSchedWins], wck[kSchedWins];
+    __shared__ int s_pos, s_cnt, s_ck, s_nw;
     const int s = blockIdx.x, H = p.H;
     const int jb = s / H, h = s - jb * H;
     const Job& job = p.jobs[jb];
@@ -36,46 +41,66 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const __grid_co
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int32_t* beg = p.chunk_beg + (size_t)job.t_row0 + (size_t)h * (size_t)len;
     const int ck_end = job.ck_begin + job.ck_count;
-    int ck = job.ck_begin;
-    int ck_pos = ck < ck_end ? p.ckpts[ck].pos : INT_MAX;
-    int pos = 0, cnt = 0;
-    while (pos < len) {
-        const int tile0 = pos;
-        const int tile_n = min(len - pos, kSchedTile + C);
-        __syncthreads();
+    if (threadIdx.x == 0) {
+        s_pos = 0;
+        s_cnt = 0;
+        s_ck = job.ck_begin;
+    }
+    __syncthreads();
+    while (s_pos < len) {
+        const int tile0 = s_pos;
+        const int tile_n = min(len - tile0, kSchedTile + C);
         for (int i = threadIdx.x; i < tile_n; i += kSchedThreads)
             sa[i] = __ldg(p.alpha + (size_t)(job.tok_begin + tile0 + i) * (size_t)H + (size_t)h);
         __syncthreads();
-        if (warp == 0) {
-            // every window that lies inside the staged tile
-            while (pos < len && pos - tile0 + min(C, len - pos) <= tile_n) {
-                int end = pos + C < len ? pos + C : len;
-                if (ck_pos < end) end = ck_pos;
-                const int win = end - pos;
-                const float a0 = lane < win ? sa[pos - tile0 + lane] : 1.f;
-                const float a1 = lane + 32 < win ? sa[pos - tile0 + lane + 32] : 1.f;
+        // every window that lies inside the staged tile
+        while (s_pos < len && s_pos - tile0 + min(C, len - s_pos) <= tile_n) {
+            if (threadIdx.x == 0) {   // the windows of a walk without cuts, from here
+                int pos = s_pos, ck = s_ck, nw = 0;
+                while (nw < kSchedWins && pos < len && pos - tile0 + min(C, len - pos) <= tile_n) {
+                    const int ck_pos = ck < ck_end ? p.ckpts[ck].pos : INT_MAX;
+                    int end = pos + C < len ? pos + C : len;
+                    if (ck_pos < end) end = ck_pos;
+                    if (ck_pos == end) ++ck;
+                    ws[nw] = pos;
+                    wl[nw] = end - pos;
+                    wck[nw] = ck;   // the checkpoint cursor after the window
+                    ++nw;
+                    pos = end;
+                }
+                s_nw = nw;
+            }
+            __syncthreads();
+            const int nw = s_nw;
+            for (int i = warp; i < nw; i += kSchedThreads / 32) {
+                const int w0 = ws[i] - tile0, win = wl[i];
+                const float a0 = lane < win ? sa[w0 + lane] : 1.f;
+                const float a1 = lane + 32 < win ? sa[w0 + lane + 32] : 1.f;
                 float g0, g1;
                 gate_prefix(a0, a1, g0, g1, lane);
                 const int first = gamma_first(g0, g1);
-                const int n = first < win ? (first > 0 ? first : 1) : win;
-                if (lane == 0) beg[cnt] = pos;
-                ++cnt;
-                pos += n;
-                if (ck_pos == pos) {
-                    ++ck;
-                    ck_pos = ck < ck_end ? p.ckpts[ck].pos : INT_MAX;
-                }
+                if (lane == 0) wn[i] = first < win ? (first > 0 ? first : 1) : win;
             }
-            if (lane == 0) {
+            __syncthreads();
+            if (threadIdx.x == 0) {   // take the windows in order up to the first cut early
+                int pos = s_pos, cnt = s_cnt, ck = s_ck;
+                for (int i = 0; i < nw; ++i) {
+                    beg[cnt++] = ws[i];
+                    if (wn[i] < wl[i]) {   // ends before its window: the cursor stays, the windows shift
+                        pos = ws[i] + wn[i];
+                        break;
+                    }
+                    pos = ws[i] + wl[i];
+                    ck = wck[i];
+                }
                 s_pos = pos;
                 s_cnt = cnt;
+                s_ck = ck;
             }
+            __syncthreads();
         }
-        __syncthreads();
-        pos = s_pos;
-        cnt = s_cnt;
     }
-    if (threadIdx.x == 0) p.chunk_cnt[s] = cnt;
+    if (threadIdx.x == 0) p.chunk_cnt[s] = s_cnt;
 }
 
 // ---- T of every chunk: 4 warps per chunk; the next chunk's K is copied in once K K^T is done, and its
