@@ -305,6 +305,35 @@ def placement_report(N: int = 8192, M: int = 16, n_requests: int = 10000):
     return out
 
 
+def two_pass_report(step, reps: int = 5):
+    """The prefill call of the timed step in both chunked variants, on the step's own inputs: the fused
+    tcgen05 scan (the default, 256-byte workspace) and the two-pass scan (chunk schedule and T of every chunk
+    first, then the scan; it needs gdn_workspace_size_two_pass bytes).  Medians of CUDA-event spans."""
+    import hybrid_model_recurrent_gb300 as gdn
+    w, inp, dev = step.w, step.inp, step.dev
+    big = torch.zeros(int(gdn.lib().gdn_workspace_size_two_pass(w.T, w.H, w.B)), dtype=torch.uint8, device=dev)
+    out = {}
+    for name, algo, ws in (("fused_ms", "chunked", step.ws), ("two_pass_ms", "two_pass", big)):
+        def call():
+            gdn.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, step.cu, ckpt_pos=step.ck, o=step.o,
+                                 S_final=step.S_final, ckpt_states=step.ckpt, ws=ws, algo=algo)
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        out[name] = float(np.median(ts))
+    out["two_pass_workspace_bytes"] = int(big.numel())
+    out["workload"] = "the timed step's prefill call (8 x 16 heads, N = 8192, 16 checkpoints)"
+    return out
+
+
 def overlap_report(dev, reps: int = 5):
     """Transfer / replay overlap ("Tail-Replay" notes page, section 2.5) on the 5 % replay workload:
     768 (layer, head) scans, tail k = 1639 of m = 32768, replayed from zero.  The transfer is the
@@ -517,6 +546,7 @@ def run_ours(args, ws, rank, local):
             "cpu_baseline": base,
             "placement": placement_report(),
             "replay_overlap": overlap_report(dev),
+            "chunked_variants": two_pass_report(step),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -497,3 +497,27 @@ def test_full_ragged_tail_replay_10pct_sampled():
     w = synth.workload("ragged10")
     samples = [(0, 0), (5, 7), (31, 15), (int(np.argmax(w.seq_lens)), 3), (int(np.argmin(w.seq_lens)), 11)]
     _replay_full("ragged10", samples)
+
+
+def test_auto_takes_two_pass_only_with_its_workspace():
+    """GDN_ALGO_AUTO runs the two-pass chunked scan when the workspace holds T of every chunk, the fused
+    chunked scan otherwise (the noalloc entry point's case); each is bit-identical to naming it."""
+    lens = [300, 129]
+    H = 2
+    w, inp = _inputs(91, lens, H, 128, 128, torch.bfloat16, 0.9, 1.0)
+    d = _dev(inp)
+    cu = w.cu_seqlens
+    ck = [[64, 150], [100]]
+    small = torch.zeros(int(gdn.lib().gdn_workspace_size()), dtype=torch.uint8, device=DEV)
+    big = torch.zeros(int(gdn.lib().gdn_workspace_size_two_pass(w.T, H, w.B)), dtype=torch.uint8, device=DEV)
+    runs = {}
+    for name, algo, ws in (("auto_small", "auto", small), ("chunked", "chunked", small), ("auto_big", "auto", big),
+                           ("two_pass", "two_pass", big)):
+        runs[name] = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=ck, algo=algo, ws=ws)
+    torch.cuda.synchronize()
+    assert gdn.read_status(ws=small) == gdn.GDN_OK and gdn.read_status(ws=big) == gdn.GDN_OK
+    for a, b in (("auto_small", "chunked"), ("auto_big", "two_pass")):
+        for key in ("o", "S_final", "ckpt_states"):
+            assert torch.equal(runs[a][key], runs[b][key]), (a, b, key)
+    with pytest.raises(gdn.GdnError):   # naming the two-pass scan with too small a workspace
+        gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, ckpt_pos=ck, algo="two_pass", ws=small)
