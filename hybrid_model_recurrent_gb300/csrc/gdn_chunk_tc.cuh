@@ -270,6 +270,22 @@ __device__ __forceinline__ int gamma_first(float g0, float g1) {
     const unsigned m1 = __ballot_sync(0xffffffffu, g1 < kGammaFloor);
     return m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : C);
 }
+// d (16 x 8) += A (16 x 16, fp32 row-major at a, row stride lda) B (16 x 8, fp32 row-major at b, row stride
+// ldb) as hi*hi, and c += hi*lo + lo*hi, every operand split x = hi + lo into bf16 (mma.sync m16n8k16, fp32
+// accumulate): half the instructions of the tf32 form for the same K; the caller adds c to d at the end
+__device__ __forceinline__ void mma_bf16x3(float (&d)[4], float (&c)[4], const float* a, int lda, const float* b,
+                                           int ldb, int g8, int t4) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    split_pair(a[g8 * lda + 2 * t4], a[g8 * lda + 2 * t4 + 1], ah[0], al[0]);
+    split_pair(a[(g8 + 8) * lda + 2 * t4], a[(g8 + 8) * lda + 2 * t4 + 1], ah[1], al[1]);
+    split_pair(a[g8 * lda + 2 * t4 + 8], a[g8 * lda + 2 * t4 + 9], ah[2], al[2]);
+    split_pair(a[(g8 + 8) * lda + 2 * t4 + 8], a[(g8 + 8) * lda + 2 * t4 + 9], ah[3], al[3]);
+    split_pair(b[(2 * t4) * ldb + g8], b[(2 * t4 + 1) * ldb + g8], bh[0], bl[0]);
+    split_pair(b[(2 * t4 + 8) * ldb + g8], b[(2 * t4 + 9) * ldb + g8], bh[1], bl[1]);
+    mma_bf16_16816(c, al, bh[0], bh[1]);
+    mma_bf16_16816(d, ah, bh[0], bh[1]);
+    mma_bf16_16816(c, ah, bl[0], bl[1]);
+}
 __device__ __forceinline__ void group_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -1119,8 +1135,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 const int mt = pw >> 2, nt = pw & 3;
                 float y[4] = {0.f, 0.f, 0.f, 0.f}, yc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32x3(y, yc, Lf + (32 + 16 * mt) * kLdF + 8 * ks, kLdF, Lf + (8 * ks) * kLdF + 8 * nt, kLdF,
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_bf16x3(y, yc, Lf + (32 + 16 * mt) * kLdF + 16 * ks, kLdF, Lf + (16 * ks) * kLdF + 8 * nt, kLdF,
                                g8, t4);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) y[e] += yc[e];
@@ -1132,8 +1148,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 group_sync(BAR_PREP, NPREP);
                 float x[4] = {0.f, 0.f, 0.f, 0.f}, xc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32x3(x, xc, Lf + (32 + 16 * mt) * kLdF + 32 + 8 * ks, kLdF, Yb + (8 * ks) * 33 + 8 * nt, 33,
+                for (int ks = 0; ks < 2; ++ks)
+                    mma_bf16x3(x, xc, Lf + (32 + 16 * mt) * kLdF + 32 + 16 * ks, kLdF, Yb + (16 * ks) * 33 + 8 * nt, 33,
                                g8, t4);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) x[e] += xc[e];
