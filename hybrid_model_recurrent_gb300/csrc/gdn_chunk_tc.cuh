@@ -1041,8 +1041,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 4 (rows 0-31 of G, columns
             //      0-31) and warp 9 (rows 32-63, columns 32-63) each take a whole diagonal 32-block of L and
             //      invert it alone: two 16x16 forward substitutions and one merge, then its T operands;
-            //      the gate warp runs a chunk ahead.  The merge within a diagonal block runs in fp32 on the
-            //      CUDA cores; the lower-left block on mma.sync tf32 (hi/lo split) over all prep warps. ----
+            //      the gate warp runs a chunk ahead.  The merges run on mma.sync with every operand split
+            //      into bf16 hi + lo (the lower-left block over all prep warps). ----
             if (pw == 0 || pw == 5) {
                 const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant: rows / columns 32 qw .. + 31
                 const int t = row, s0 = 32 * half;         // warp 4: t 0-31, s 0-31; warp 9: t 32-63, s 32-63
@@ -1064,41 +1064,42 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         for (int r = 0; r < 16; ++r) Lf[(16 * bb + r) * kLdF + 16 * bb + jc] = x[r];
                     }
                     __syncwarp();
-                    // merge: T_ib,jb = -T_ib,ib (L_ib,jb T_jb,jb), (jb, ib) = (2 qw, 2 qw + 1), in fp32 on the CUDA
-                    // cores (the tensor pipe is busy with the chain's products): lane = column c, half = 8 rows
+                    // merge: T_ib,jb = -T_ib,ib (L_ib,jb T_jb,jb), (jb, ib) = (2 qw, 2 qw + 1), bf16 hi/lo x 3 on
+                    // mma.sync (two 8-column tiles, one k step each)
                     {
-                        const int jb = 2 * qw, ib = jb + 1, c = lane & 15, rh = lane >> 4;
-                        const float* Lij = Lf + (16 * ib) * kLdF + 16 * jb;
-                        const float* Tjj = Lf + (16 * jb) * kLdF + 16 * jb;
-                        const float* Tii = Lf + (16 * ib) * kLdF + 16 * ib;
-                        float y[8];
+                        const int jb = 2 * qw, ib = jb + 1, g8 = lane >> 2, t4 = lane & 3;
+                        float* sc = Ld + jb * 16 * 17;   // this warp's diagonal blocks of L are no longer needed
+                        float y[2][4], yc[2][4];
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) y[r] = 0.f;
+                        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float tk = Tjj[k * kLdF + c];
-#pragma unroll
-                            for (int r = 0; r < 8; ++r) y[r] = fmaf(Lij[(8 * rh + r) * kLdF + k], tk, y[r]);
+                            for (int e = 0; e < 4; ++e) y[nt][e] = yc[nt][e] = 0.f;
+                            mma_bf16x3(y[nt], yc[nt], Lf + (16 * ib) * kLdF + 16 * jb, kLdF,
+                                       Lf + (16 * jb) * kLdF + 16 * jb + 8 * nt, kLdF, g8, t4);
                         }
-                        float ylo[8], yhi[8];   // column c of L_ib,jb T_jb,jb, rows 0-7 and 8-15
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const float o = __shfl_xor_sync(0xffffffffu, y[r], 16);
-                            ylo[r] = rh ? o : y[r];
-                            yhi[r] = rh ? y[r] : o;
+                        for (int nt = 0; nt < 2; ++nt) {
+                            sc[g8 * 16 + 8 * nt + 2 * t4] = y[nt][0] + yc[nt][0];
+                            sc[g8 * 16 + 8 * nt + 2 * t4 + 1] = y[nt][1] + yc[nt][1];
+                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4] = y[nt][2] + yc[nt][2];
+                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4 + 1] = y[nt][3] + yc[nt][3];
                         }
-                        float x[8];
+                        __syncwarp();
+                        float x[2][4], xc[2][4];
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) x[r] = 0.f;
+                        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float yk = k < 8 ? ylo[k] : yhi[k - 8];
-#pragma unroll
-                            for (int r = 0; r < 8; ++r) x[r] = fmaf(Tii[(8 * rh + r) * kLdF + k], yk, x[r]);
+                            for (int e = 0; e < 4; ++e) x[nt][e] = xc[nt][e] = 0.f;
+                            mma_bf16x3(x[nt], xc[nt], Lf + (16 * ib) * kLdF + 16 * ib, kLdF, sc + 8 * nt, 16, g8, t4);
                         }
-                        __syncwarp();   // every lane is done with L_ib,jb
+                        float* dst = Lf + (16 * ib) * kLdF + 16 * jb;
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) Lf[(16 * ib + 8 * rh + r) * kLdF + 16 * jb + c] = -x[r];
+                        for (int nt = 0; nt < 2; ++nt) {
+                            dst[g8 * kLdF + 8 * nt + 2 * t4] = -(x[nt][0] + xc[nt][0]);
+                            dst[g8 * kLdF + 8 * nt + 2 * t4 + 1] = -(x[nt][1] + xc[nt][1]);
+                            dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4] = -(x[nt][2] + xc[nt][2]);
+                            dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4 + 1] = -(x[nt][3] + xc[nt][3]);
+                        }
                     }
                     __syncwarp();
                     // this 32-block's T operands: row t, columns s0 .. s0 + 31, 8 columns per 16-byte store

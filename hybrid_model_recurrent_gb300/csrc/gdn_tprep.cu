@@ -8,7 +8,7 @@
 //   schedule_kernel - the chunk starts of each (job, head): windows of 64 tokens from the previous
 //       chunk end, cut at the next checkpoint and before the token where gamma falls below 2^-32
 //       (the rule the scan kernel's gate warp applies, with the same rounding);
-//   tprep_kernel    - T of every chunk in fp32 (tf32 x 3 merges on mma.sync, K K^T on bf16 mma.sync), stored
+//   tprep_kernel    - T of every chunk in fp32 (bf16 hi/lo x 3 merges and K K^T on mma.sync), stored
 //       as the scan's MMA operands T diag(beta gamma) and T diag(beta), each split into bf16 hi + lo, in rows
 //       indexed by token, so the storage is bounded by the tokens scanned.
 #include <cuda_runtime.h>
@@ -295,11 +295,8 @@ __global__ void __launch_bounds__(kTpThreads, kTpBlocksPerSm) tprep_kernel(const
             const int pr = warp >> 1, hf = warp & 1, jb = 2 * pr, ib = jb + 1;
             float* yp = sy + pr * 256;   // [16][16]
             float y[4] = {0.f, 0.f, 0.f, 0.f}, yc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks)
-                if (ks >= hf)   // T_jb,jb is zero above its diagonal
-                    mma_tf32x3(y, yc, sl + (16 * ib) * kTpLd + 16 * jb + 8 * ks, kTpLd,
-                               sl + (16 * jb + 8 * ks) * kTpLd + 16 * jb + 8 * hf, kTpLd, g8, t4);
+            mma_bf16x3(y, yc, sl + (16 * ib) * kTpLd + 16 * jb, kTpLd, sl + (16 * jb) * kTpLd + 16 * jb + 8 * hf, kTpLd,
+                       g8, t4);
 #pragma unroll
             for (int e = 0; e < 4; ++e) y[e] += yc[e];
             yp[g8 * 16 + 8 * hf + 2 * t4] = y[0];
@@ -308,10 +305,7 @@ __global__ void __launch_bounds__(kTpThreads, kTpBlocksPerSm) tprep_kernel(const
             yp[(g8 + 8) * 16 + 8 * hf + 2 * t4 + 1] = y[3];
             __syncthreads();   // every read of L_ib,jb is done before T_ib,jb overwrites it
             float xx[4] = {0.f, 0.f, 0.f, 0.f}, xc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks)
-                mma_tf32x3(xx, xc, sl + (16 * ib) * kTpLd + 16 * ib + 8 * ks, kTpLd, yp + 8 * ks * 16 + 8 * hf, 16, g8,
-                           t4);
+            mma_bf16x3(xx, xc, sl + (16 * ib) * kTpLd + 16 * ib, kTpLd, yp + 8 * hf, 16, g8, t4);
             float* dst = sl + (16 * ib) * kTpLd + 16 * jb + 8 * hf;
             dst[g8 * kTpLd + 2 * t4] = -(xx[0] + xc[0]);
             dst[g8 * kTpLd + 2 * t4 + 1] = -(xx[1] + xc[1]);
@@ -327,12 +321,12 @@ __global__ void __launch_bounds__(kTpThreads, kTpBlocksPerSm) tprep_kernel(const
 #pragma unroll
                 for (int e = 0; e < 4; ++e) y[mt][e] = yc[mt][e] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                if (ks < warp) continue;   // rows of T_AA above column 8w are zero
+            for (int ks = 0; ks < 2; ++ks) {
+                if (16 * ks + 15 < 8 * warp) continue;   // rows of T_AA above column 8w are zero
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt)
-                    mma_tf32x3(y[mt], yc[mt], sl + (32 + 16 * mt) * kTpLd + 8 * ks, kTpLd,
-                               sl + (8 * ks) * kTpLd + 8 * warp, kTpLd, g8, t4);
+                    mma_bf16x3(y[mt], yc[mt], sl + (32 + 16 * mt) * kTpLd + 16 * ks, kTpLd,
+                               sl + (16 * ks) * kTpLd + 8 * warp, kTpLd, g8, t4);
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
@@ -347,9 +341,9 @@ __global__ void __launch_bounds__(kTpThreads, kTpBlocksPerSm) tprep_kernel(const
             for (int mt = 0; mt < 2; ++mt) {
                 float xx[4] = {0.f, 0.f, 0.f, 0.f}, xc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    if (ks > 2 * mt + 1) continue;   // T_BB is zero above its diagonal
-                    mma_tf32x3(xx, xc, sl + (32 + 16 * mt) * kTpLd + 32 + 8 * ks, kTpLd, sy + (8 * ks) * 33 + 8 * warp,
+                for (int ks = 0; ks < 2; ++ks) {
+                    if (ks > mt) continue;   // T_BB is zero above its diagonal
+                    mma_bf16x3(xx, xc, sl + (32 + 16 * mt) * kTpLd + 32 + 16 * ks, kTpLd, sy + (16 * ks) * 33 + 8 * warp,
                                33, g8, t4);
                 }
                 float* dst = sl + (32 + 16 * mt) * kTpLd + 8 * warp + 2 * t4;
