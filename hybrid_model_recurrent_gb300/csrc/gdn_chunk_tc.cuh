@@ -1040,12 +1040,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             };
             // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 4 (rows 0-31 of G, columns
             //      0-31) and warp 9 (rows 32-63, columns 32-63) each take a whole diagonal 32-block of L and
-            //      invert it alone: two 16x16 forward substitutions and one merge, then its T operands;
-            //      the gate warp runs a chunk ahead.  The merges run on mma.sync with every operand split
-            //      into bf16 hi + lo (the lower-left block over all prep warps). ----
+            //      invert it alone: two 16x16 forward substitutions and one merge; the gate warp runs a
+            //      chunk ahead.  Then the whole group writes the T operands of both diagonal blocks and merges
+            //      the lower-left block.  The merges run on mma.sync with every operand split into bf16
+            //      hi + lo. ----
             if (pw == 0 || pw == 5) {
                 const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant: rows / columns 32 qw .. + 31
-                const int t = row, s0 = 32 * half;         // warp 4: t 0-31, s 0-31; warp 9: t 32-63, s 32-63
                 {
                     // lanes 0-15: column jc of block 2 qw; lanes 16-31: of block 2 qw + 1 (forward substitution,
                     // each dot product in four partial sums)
@@ -1101,37 +1101,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                             dst[(g8 + 8) * kLdF + 8 * nt + 2 * t4 + 1] = -(x[nt][3] + xc[nt][3]);
                         }
                     }
-                    __syncwarp();
-                    // this 32-block's T operands: row t, columns s0 .. s0 + 31, 8 columns per 16-byte store
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 x0 = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + 8 * q);
-                        const float4 x1 = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + 8 * q + 4);
-                        const float4 a0 = *reinterpret_cast<const float4*>(sg_bg + s0 + 8 * q);
-                        const float4 a1 = *reinterpret_cast<const float4*>(sg_bg + s0 + 8 * q + 4);
-                        const float4 b0 = *reinterpret_cast<const float4*>(sg_b + s0 + 8 * q);
-                        const float4 b1 = *reinterpret_cast<const float4*>(sg_b + s0 + 8 * q + 4);
-                        uint32_t h1[4], l1[4], h2[4], l2[4];
-                        split_pair(x0.x * a0.x, x0.y * a0.y, h1[0], l1[0]);
-                        split_pair(x0.z * a0.z, x0.w * a0.w, h1[1], l1[1]);
-                        split_pair(x1.x * a1.x, x1.y * a1.y, h1[2], l1[2]);
-                        split_pair(x1.z * a1.z, x1.w * a1.w, h1[3], l1[3]);
-                        split_pair(x0.x * b0.x, x0.y * b0.y, h2[0], l2[0]);
-                        split_pair(x0.z * b0.z, x0.w * b0.w, h2[1], l2[1]);
-                        split_pair(x1.x * b1.x, x1.y * b1.y, h2[2], l2[2]);
-                        split_pair(x1.z * b1.z, x1.w * b1.w, h2[3], l2[3]);
-                        const uint32_t o = sw128(t, s0 + 8 * q);
-                        *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-                        *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-                        *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-                        *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
-                    }
                 }
             } else if (pw == 3 && !last) {
                 compute_chunk(j + 1);   // the gate warp runs one chunk ahead
             }
             group_sync(BAR_PREP, NPREP);
-            {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block on mma.sync tf32; warp = (row, column) tile
+            {   // the diagonal 32-blocks' T operands, spread over the whole group: one row piece of 8 columns
+                // (one 16-byte store per plane) per thread
+                const int t = 32 * (ptid >> 7) + ((ptid >> 2) & 31), s0 = 32 * (ptid >> 7) + 8 * (ptid & 3);
+                const float4 x0 = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0);
+                const float4 x1 = *reinterpret_cast<const float4*>(Lf + t * kLdF + s0 + 4);
+                const float4 a0 = *reinterpret_cast<const float4*>(sg_bg + s0);
+                const float4 a1 = *reinterpret_cast<const float4*>(sg_bg + s0 + 4);
+                const float4 b0 = *reinterpret_cast<const float4*>(sg_b + s0);
+                const float4 b1 = *reinterpret_cast<const float4*>(sg_b + s0 + 4);
+                uint32_t h1[4], l1[4], h2[4], l2[4];
+                split_pair(x0.x * a0.x, x0.y * a0.y, h1[0], l1[0]);
+                split_pair(x0.z * a0.z, x0.w * a0.w, h1[1], l1[1]);
+                split_pair(x1.x * a1.x, x1.y * a1.y, h1[2], l1[2]);
+                split_pair(x1.z * a1.z, x1.w * a1.w, h1[3], l1[3]);
+                split_pair(x0.x * b0.x, x0.y * b0.y, h2[0], l2[0]);
+                split_pair(x0.z * b0.z, x0.w * b0.w, h2[1], l2[1]);
+                split_pair(x1.x * b1.x, x1.y * b1.y, h2[2], l2[2]);
+                split_pair(x1.z * b1.z, x1.w * b1.w, h2[3], l2[3]);
+                const uint32_t o = sw128(t, s0);
+                *reinterpret_cast<uint4*>(smem + OFF_T1H + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_T1L + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_T2H + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                *reinterpret_cast<uint4*>(smem + OFF_T2L + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+            }
+            {   // T_BA = -T_BB (L_BA T_AA) for the lower-left 32x32 block; warp = (row, column) tile
                 const int g8 = lane >> 2, t4 = lane & 3;
                 const int mt = pw >> 2, nt = pw & 3;
                 float y[4] = {0.f, 0.f, 0.f, 0.f}, yc[4] = {0.f, 0.f, 0.f, 0.f};
