@@ -817,10 +817,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 
         // chunk jj's K/Q landed and its rows past the chunk zeroed; then [K; Q] K^T can be issued
         auto stage_kq = [&](int jj) -> bool {
+            tc_fence_before();   // the G columns were last read by the previous chunk's P extraction
             if (!group_wait(&bar_kq[jj & 1], (uint32_t)((jj >> 1) & 1), leader, BAR_PREP, NPREP, abort_flag, limit))
                 return false;
             const int nn = ring[jj % kRing].n;
-            if (nn < C) {
+            if (nn < C) {   // a full chunk needs no barrier beyond the wait's own
                 const int nz = C - nn;
                 for (int i = ptid; i < 4 * nz * 8; i += NPREP) {
                     const int seg = i & 7, rz = (i >> 3) % nz, part = (i >> 3) / nz;   // K / Q x two column blocks
@@ -828,9 +829,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     *reinterpret_cast<uint4*>(base + (nn + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 proxy_fence();
+                group_sync(BAR_PREP, NPREP);
             }
-            tc_fence_before();   // the G columns were last read by the previous chunk's P extraction
-            group_sync(BAR_PREP, NPREP);
             if (leader) mbar_arrive(bar_gin);
             return true;
         };
@@ -921,8 +921,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         *reinterpret_cast<uint4*>(base + (n + rz) * 128 + seg * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
                     proxy_fence();
+                    group_sync(BAR_PREP, NPREP);   // a full chunk's tiles are all the copies' own
                 }
-                group_sync(BAR_PREP, NPREP);
                 if (leader) mbar_arrive(bar_wuin);
                 if (pw == 3 && !last) compute_chunk(j + 1);   // the gate warp runs one chunk ahead, off the barriers
 
@@ -1156,7 +1156,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 put_t12(32 + 16 * mt + g8, 8 * nt + 2 * t4, -x[0], -x[1]);
                 put_t12(32 + 16 * mt + g8 + 8, 8 * nt + 2 * t4, -x[2], -x[3]);
             }
-            // ---- this chunk's V (rows past the chunk zeroed): landed while T was formed ----
+            // ---- this chunk's V (rows past the chunk zeroed): landed while T was formed.  The T operand
+            //      stores are made visible to the MMA by the wait's own barrier (one more for padding) ----
+            proxy_fence();
             if (!group_wait(bar_v, (uint32_t)(j & 1), leader, BAR_PREP, NPREP, abort_flag, limit)) break;
             if (n < C) {
                 const int nz = C - n;
@@ -1165,9 +1167,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     *reinterpret_cast<uint4*>(smem + OFF_V + part * 8192 + (n + rz) * 128 + seg * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
+                proxy_fence();
+                group_sync(BAR_PREP, NPREP);
             }
-            proxy_fence();
-            group_sync(BAR_PREP, NPREP);
             if (leader) mbar_arrive(bar_wuin);
 
             // ---- while W^T and U~^T are computed: P = mask(q_t . k_s) from the Q rows of [K; Q] K^T, once the
