@@ -164,6 +164,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// two 32-column pieces for one wait: the second load's latency hides behind the first's (one asm, so no
+// register is read before the wait)
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va)[32], float (&vb)[32]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+        "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+          "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]),
+          "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
+          "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[32 + i]);
+    }
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
@@ -494,10 +521,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             float* d1 = (fold && Rp->dump_slot >= 0)
                             ? p.ckpt_states + (size_t)Rp->dump_slot * (size_t)H * D * D + head_state
                             : nullptr;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                float v[32];
-                tmem_ld32(trow + T_S + 32 * cb, v);
+            auto split_block = [&](int cb, float(&v)[32]) {
                 if (fold) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= ff;
@@ -513,6 +537,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= f;
                     tmem_st32(trow + T_S + 32 * cb, v);
+                }
+            };
+            if constexpr (PRE_T) {   // two 32-column blocks per TMEM round trip (in the fused kernel the
+                                     // extra registers cost more than the round trip saves)
+#pragma unroll 1
+                for (int cp = 0; cp < 2; ++cp) {
+                    float v2[2][32];
+                    tmem_ld32x2(trow + T_S + 64 * cp, trow + T_S + 64 * cp + 32, v2[0], v2[1]);
+                    split_block(2 * cp, v2[0]);
+                    split_block(2 * cp + 1, v2[1]);
+                }
+            } else {
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    float v[32];
+                    tmem_ld32(trow + T_S + 32 * cb, v);
+                    split_block(cb, v);
                 }
             }
             tmem_st_wait();
@@ -545,9 +586,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             OutT* stg = reinterpret_cast<OutT*>(smem + OFF_OST + lq * 2048);
             constexpr int kTok = 2048 / (32 * (int)sizeof(OutT));   // tokens per staged tile: 32 bf16, 16 fp32
             constexpr int kSeg = 32 * (int)sizeof(OutT) / 16;        // 16-byte pieces per token and warp
-#pragma unroll 1
-            for (int cb = 0; cb < 2 && 32 * cb < n; ++cb) {
-                float v[32], rs[32];
+            float vo[2][32];
+            tmem_ld32x2(trow + TO, trow + TO + 32, vo[0], vo[1]);
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                if (32 * cb >= n) break;
+                float(&v)[32] = vo[cb];
+                float rs[32];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
                     const float4 x = *reinterpret_cast<const float4*>(&R.rs[32 * cb + i]);
@@ -556,7 +601,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     rs[i + 2] = x.z;
                     rs[i + 3] = x.w;
                 }
-                tmem_ld32(trow + TO + 32 * cb, v);
                 if (cb == 0 && single) v[0] = fmaf(qk0, u0, rs[0] * v[0]);
                 else if (cb == 0) v[0] *= rs[0];
 #pragma unroll
@@ -649,10 +693,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         c[i + 2] = x.z;
                         c[i + 3] = x.w;
                     }
-                    tmem_ld32(trow + T_U + 32 * cb, v);
                     {
                         float w[32];
-                        tmem_ld32(trow + TW + 32 * cb, w);
+                        tmem_ld32x2(trow + T_U + 32 * cb, trow + TW + 32 * cb, v, w);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] += w[i];
                     }
