@@ -51,12 +51,14 @@ SM_MAX_MHZ = 2070.0
 PEAK_ALU_TFLOPS = SM_COUNT * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12  # 80.54
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_chunk_tc_kernel_prefill_8x16x8192.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_chunk_tc_kernel_step_8x16x8192.md")
 KERNEL_SRC = os.path.join(ROOT, "hybrid_model_recurrent_gb300", "csrc", "gdn_chunk_tc.cuh")
 # tcgen05.mma MACs per 64-token chunk and head in the chunked kernel: 76 MMAs of 128x64x16
 # ([K;Q] K^T 8, W^T and U~^T 16, S_0 (-W)^T and S_0 Q^T 40, U''^T P''^T 12) and 8 of 128x128x16
 # (the state update)
 CHUNK_MACS = 76 * 128 * 64 * 16 + 8 * 128 * 128 * 16
+# without a readout the S_0 Q^T and U''^T P^T products (16 + 12 of 128x64x16) are not issued
+CHUNK_MACS_NO_READOUT = CHUNK_MACS - 28 * 128 * 64 * 16
 
 
 def measured_peaks():
@@ -190,12 +192,18 @@ class Step:
         self.o = torch.empty((T, H, dv), dtype=w.out_dtype, device=device)
         self.S_final = torch.empty((B, H, dv, dk), dtype=f32, device=device)
         n_ck = sum(len(c) for c in self.ck)
-        self.ckpt = torch.empty((n_ck, H, dv, dk), dtype=f32, device=device)
+        # The checkpoint store, two buffers: a step's prefill writes one while its resumes read the other,
+        # written by the step before (as a serving step resumes requests from checkpoints stored earlier;
+        # every step processes the same batch, so both buffers end up holding the same states).
+        self.ck_store = [torch.empty((n_ck, H, dv, dk), dtype=f32, device=device) for _ in range(2)]
+        self.n_runs = 0
+        self.ckpt = self.ck_store[0]
         self.chosen = []
-        rows = 0
+        self.resume_lens = []
         for s, d in self.probes:
             j = gdn.gdn_select_ckpt(self.ck[s], d)
-            rows += d - (0 if j < 0 else self.ck[s][j])
+            self.resume_lens.append(d - (0 if j < 0 else self.ck[s][j]))
+        rows = sum(self.resume_lens)
         self.resume_rows = rows
         self.o_res = torch.empty((max(rows, 1), H, dv), dtype=w.out_dtype, device=device)
         self.S_out = torch.empty((len(self.probes), H, dv, dk), dtype=f32, device=device)
@@ -203,25 +211,45 @@ class Step:
         self.replay_tokens = sum(gdn.gdn_replay_plan(m, *REPLAY_R)[1] for m in self.m)
         self.tok_head = {"prefill": T * H, "resume": rows * H, "replay": self.replay_tokens * H}
         self.ws = gdn.workspace(device)
-        self.launches_per_step = 3
+        self.launches_per_step = 1
         self.ev = None
+        # the store the first step's resumes read (untimed)
+        gdn.gdn_prefill_ckpt(self.inp.q, self.inp.k, self.inp.v, self.inp.alpha, self.inp.beta, self.cu,
+                             ckpt_pos=self.ck, o=self.o, S_final=self.S_final, ckpt_states=self.ck_store[1],
+                             ws=self.ws)
 
     def units(self) -> int:
         return sum(self.tok_head.values())
 
     def run(self, inp=None, record=None):
+        """The step: the batch's prefill (readout + checkpoints), the resume probes (from the checkpoint
+        store of the step before) and the tail replays, one gdn_step launch."""
         g = self.gdn
         inp = inp or self.inp
         s = torch.cuda.current_stream(self.dev)
+        write, read = self.ck_store[self.n_runs & 1], self.ck_store[(self.n_runs + 1) & 1]
+        self.n_runs += 1
+        self.ckpt = write
         if record is not None:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(s)
-        g.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, ckpt_pos=self.ck, o=self.o,
-                           S_final=self.S_final, ckpt_states=self.ckpt, ws=self.ws)
+        g.gdn_step(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, ws=self.ws,
+                   prefill=dict(ckpt_pos=self.ck, o=self.o, S_final=self.S_final, ckpt_states=write),
+                   resume=dict(ckpt_states=read, ckpt_pos=self.ck, probes=self.probes, o_out=self.o_res,
+                               S_out=self.S_out),
+                   replay=dict(m=self.m, r_num=REPLAY_R[0], r_den=REPLAY_R[1], S_hat=self.S_hat))
         if record is not None:
             e1.record(s)
             record.append((e0, e1))
+
+    def run_three_calls(self, inp=None):
+        """The same step as three launches, one per entry point, each resume reading the checkpoints its own
+        step's prefill has just written."""
+        g = self.gdn
+        inp = inp or self.inp
+        g.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, ckpt_pos=self.ck, o=self.o,
+                           S_final=self.S_final, ckpt_states=self.ckpt, ws=self.ws)
         g.gdn_resume_from_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, self.ckpt, self.ck, self.probes,
                                o_out=self.o_res, S_out=self.S_out, ws=self.ws)
         g.gdn_tail_replay(None, inp.k, inp.v, inp.alpha, inp.beta, self.cu, self.m, *REPLAY_R, S_hat=self.S_hat,
@@ -334,6 +362,29 @@ def two_pass_report(step, reps: int = 5):
     return out
 
 
+def step_forms_report(step, reps: int = 20):
+    """The timed step as one gdn_step launch against the three entry points one after another (medians of
+    CUDA-event spans over one step each)."""
+    dev = step.dev
+    out = {}
+    for name, fn in (("one_launch_ms", step.run), ("three_calls_ms", step.run_three_calls)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        out[name] = float(np.median(ts))
+    out["note"] = ("one launch: the prefill's 128 (sequence, head) jobs take 128 of the 152 SMs and the short "
+                   "resume and replay jobs run on the other 24 during it")
+    return out
+
+
 def overlap_report(dev, reps: int = 5):
     """Transfer / replay overlap ("Tail-Replay" notes page, section 2.5) on the 5 % replay workload:
     768 (layer, head) scans, tail k = 1639 of m = 32768, replayed from zero.  The transfer is the
@@ -406,6 +457,7 @@ def config_dict(w, ws):
             "seqs_per_rank": w.B, "heads": w.H, "seq_len": w.seq_lens[0], "d_k": w.dk, "d_v": w.dv,
             "ckpts_per_seq": len(w.ckpt_positions()[0]), "resume_probes": N_PROBES,
             "replay_r": f"{REPLAY_R[0]}/{REPLAY_R[1]}", "parallelism": f"dp{ws} (weak: one batch per rank)",
+            "step": "one gdn_step launch; the resumes read the checkpoint store written by the step before",
             "l2": "inputs larger than L2 (805 MB of bf16 q/k/v streamed per step)", "seed": 0}
 
 
@@ -477,7 +529,7 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status {gdn.status_string(status)} during the timed region")
     units = step.units() * args.steps
     total, slowest, thr = aggregate(units, elapsed, ws, dev)
-    prefill_ms = statistics.mean(a.elapsed_time(b) for a, b in rec)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in rec)
 
     # ---- end to end: pinned host inputs in, every result out, each step ----
     host_in = [t.cpu().pin_memory() for t in (step.inp.q, step.inp.k, step.inp.v, step.inp.alpha, step.inp.beta)]
@@ -553,17 +605,25 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     _, _, e2e_thr = aggregate(step.units() * e2e_steps, e2e_el, ws, dev)
 
-    flops_per_launch = 3 * w.dv * w.dk * 2 * w.T * w.H   # 3 FMAs per state element per tok*head
-    # algorithmic bytes per tok*head: q, k, v (bf16) + alpha, beta (fp32) + o (bf16)
-    # + the checkpoint and final states amortised over the sequence
+    # The step's one launch: algorithmic bytes and the method's flops of its three kinds of jobs
+    # (per tok*head: q, k, v bf16 768 B + alpha, beta 8 B + o bf16 256 B with a readout, k, v and gates 520 B
+    # without; states read or written once each, 64 KiB per (range, head)).
+    D = w.dv * w.dk
     es = 2
     n_ck = len(step.ck[0])
-    bytes_tok_head = (2 * w.dk + w.dv) * es + 8 + w.dv * es + (n_ck + 1) * w.dv * w.dk * 4 / w.seq_lens[0]
-    bytes_per_launch = bytes_tok_head * w.T * w.H
-    achieved_gbs = bytes_per_launch / (prefill_ms * 1e-3) / 1e9
+    pf_th, rs_th, rp_th = step.tok_head["prefill"], step.tok_head["resume"], step.tok_head["replay"]
+    bytes_pf = pf_th * ((2 * w.dk + w.dv) * es + 8 + w.dv * es) + w.B * w.H * (n_ck + 1) * D * 4
+    bytes_rs = rs_th * ((2 * w.dk + w.dv) * es + 8 + w.dv * es) + len(step.probes) * w.H * 2 * D * 4
+    bytes_rp = rp_th * ((w.dk + w.dv) * es + 8) + w.B * w.H * D * 4
+    bytes_per_launch = bytes_pf + bytes_rs + bytes_rp
+    flops_per_launch = 6 * D * (pf_th + rs_th) + 4 * D * rp_th   # 3 (2 without a readout) FMAs per element
+    launch_s = launch_ms * 1e-3
+    achieved_gbs = bytes_per_launch / launch_s / 1e9
     hbm_peak, bf16_peak, peak_src = measured_peaks()
-    chunks = w.B * w.H * ((w.seq_lens[0] + 63) // 64)
-    mma_flops = chunks * CHUNK_MACS * 2
+    ch = lambda n: (n + 63) // 64
+    chunks_rd = w.B * w.H * ch(w.seq_lens[0]) + w.H * sum(ch(n) for n in step.resume_lens)
+    chunks_nr = w.H * sum(ch(gdn.gdn_replay_plan(m, *REPLAY_R)[1]) for m in step.m)
+    mma_flops = 2 * (chunks_rd * CHUNK_MACS + chunks_nr * CHUNK_MACS_NO_READOUT)
     base = cpu_baseline(w) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
     if rank == 0:
         line = {
@@ -576,19 +636,23 @@ def run_ours(args, ws, rank, local):
                     "serial_value": e2e_serial_thr / 1e6,
                     "steps": e2e_steps},
             "gpu_launches": step.launches_per_step * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "gdn_chunk_tc_kernel<bf16 out, readout> (prefill)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "gdn_chunk_tc_kernel<bf16 out, readout> (the step's one launch: prefill, "
+                                   "resume and tail-replay jobs)",
                          "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved_gbs / hbm_peak, "traffic": profile_traffic(),
-                         "launch_ms": prefill_ms, "algorithmic_bytes_per_launch": bytes_per_launch,
-                         "algorithmic_bytes_per_tok_head": bytes_tok_head,
+                         "launch_ms": launch_ms, "algorithmic_bytes_per_launch": bytes_per_launch,
+                         "algorithmic_bytes": {"prefill": bytes_pf, "resume": bytes_rs, "replay": bytes_rp,
+                                               "per_tok_head": "1032 with a readout, 520 without; + 64 KiB per "
+                                                               "state read or written"},
                          "peak_source": f"hbm_gbs of MEASURED_PEAKS.json ({peak_src})",
-                         "tensor_view": {"executed_mma_tflops": mma_flops / (prefill_ms * 1e-3) / 1e12,
+                         "tensor_view": {"executed_mma_tflops": mma_flops / launch_s / 1e12,
                                          "peak_bf16_tflops": bf16_peak,
-                                         "frac": mma_flops / (prefill_ms * 1e-3) / 1e12 / bf16_peak},
+                                         "frac": mma_flops / launch_s / 1e12 / bf16_peak},
                          "fp32_alu_equivalent": {
-                             "algorithmic_tflops": flops_per_launch / (prefill_ms * 1e-3) / 1e12,
+                             "algorithmic_tflops": flops_per_launch / launch_s / 1e12,
                              "peak_tflops": PEAK_ALU_TFLOPS,
-                             "frac": flops_per_launch / (prefill_ms * 1e-3) / 1e12 / PEAK_ALU_TFLOPS,
+                             "frac": flops_per_launch / launch_s / 1e12 / PEAK_ALU_TFLOPS,
                              "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"}},
             "phases": {k: v for k, v in step.tok_head.items()},
             "states_per_s": sum(len(c) for c in step.ck) * w.H * args.steps / slowest,
@@ -596,6 +660,7 @@ def run_ours(args, ws, rank, local):
             "placement": placement_report(),
             "replay_overlap": overlap_report(dev),
             "chunked_variants": two_pass_report(step),
+            "step_forms": step_forms_report(step),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

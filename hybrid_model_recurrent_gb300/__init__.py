@@ -8,6 +8,7 @@ the caller does not pass are allocated here.  The names follow the C ABI in
 * ``gdn_prefill_ckpt``      prefill with exact state dumps at sparse positions
 * ``gdn_resume_from_ckpt``  resume at overlap depth d from the deepest stored state
 * ``gdn_tail_replay``       Tail-Replay from a zero state at a = m - ceil(r m)
+* ``gdn_step``              the three above for one serving step, in one launch
 * host helpers ``gdn_replay_plan``, ``gdn_select_ckpt``, status utilities.
 
 There is no fallback: if the compiled library is missing the import of a
@@ -39,6 +40,26 @@ _workspaces: Dict[int, torch.Tensor] = {}
 class _Group(ctypes.Structure):
     _fields_ = [("layers", ctypes.c_int32), ("heads", ctypes.c_int32), ("d_model", ctypes.c_int32),
                 ("d_head", ctypes.c_int32)]
+
+
+_vp, _pi64 = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64)
+
+
+class _PrefillArgs(ctypes.Structure):
+    _fields_ = [("S0", _vp), ("o", _vp), ("S_final", _vp), ("ckpt_pos", _pi64), ("cu_ckpt", _pi64),
+                ("ckpt_states", _vp)]
+
+
+class _ResumeArgs(ctypes.Structure):
+    _fields_ = [("S0", _vp), ("ckpt_states", _vp), ("ckpt_pos", _pi64), ("cu_ckpt", _pi64),
+                ("num_probes", ctypes.c_int32), ("probe_seq", ctypes.POINTER(ctypes.c_int32)),
+                ("probe_depth", _pi64), ("S_out", _vp), ("o_out", _vp), ("chosen_pos", _pi64),
+                ("o_offsets", _pi64)]
+
+
+class _ReplayArgs(ctypes.Structure):
+    _fields_ = [("m", _pi64), ("r_num", ctypes.c_int32), ("r_den", ctypes.c_int32), ("S_a", _vp), ("S_hat", _vp),
+                ("S_exact", _vp), ("o", _vp), ("a_out", _pi64), ("k_out", _pi64)]
 
 
 class GdnError(RuntimeError):
@@ -75,6 +96,8 @@ def lib():
                                                pi64, pi64, vp, sz, vp]
             L.gdn_tail_replay.argtypes = [P, vp, vp, vp, vp, vp, pi64, i32, i32, vp, vp, vp, vp, pi64, pi64, vp, sz,
                                           vp]
+            L.gdn_step.argtypes = [P, vp, vp, vp, vp, vp, ctypes.POINTER(_PrefillArgs), ctypes.POINTER(_ResumeArgs),
+                                   ctypes.POINTER(_ReplayArgs), vp, sz, vp]
             L.gdn_replay_plan.argtypes = [i64, i32, i32, pi64, pi64]
             L.gdn_select_ckpt.argtypes = [pi64, i32, i64, pi32]
             L.gdn_tail_replay_k.argtypes = [P, vp, vp, vp, vp, vp, pi64, pi64, vp, vp, vp, vp, vp, sz, vp]
@@ -99,7 +122,7 @@ def lib():
             L.gdn_debug_stall_after.restype = None
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_status_string.restype = ctypes.c_char_p
-            for f in ("gdn_prefill_ckpt", "gdn_resume_from_ckpt", "gdn_tail_replay", "gdn_replay_plan",
+            for f in ("gdn_prefill_ckpt", "gdn_resume_from_ckpt", "gdn_tail_replay", "gdn_step", "gdn_replay_plan",
                       "gdn_select_ckpt", "gdn_clear_status", "gdn_read_status"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
@@ -366,6 +389,110 @@ def gdn_tail_replay(q, k, v, alpha, beta, cu_seqlens, m, r_num: int, r_den: int,
     _check(rc, "gdn_tail_replay")
     return {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o, "a": a_out.tolist(),
             "k": k_out.tolist()}
+
+
+def gdn_step(q, k, v, alpha, beta, cu_seqlens, *, prefill: Optional[dict] = None, resume: Optional[dict] = None,
+             replay: Optional[dict] = None, out_dtype: Optional[torch.dtype] = None, stream=None,
+             ws: Optional[torch.Tensor] = None, algo: str = "auto"):
+    """One serving step in one launch: any of a prefill, resumes and tail replays over the same streams.
+
+    prefill: dict(ckpt_pos=None, S0=None, readout=True, o=None, S_final=None, ckpt_states=None)
+    resume:  dict(ckpt_states, ckpt_pos, probes, S0=None, readout=True, S_out=None, o_out=None); the
+             checkpoints must come from an earlier call (this call's prefill may not write them)
+    replay:  dict(m, r_num, r_den, S_a=None, readout=False, S_hat=None, S_exact=None, o=None)
+    Returns dict(prefill=..., resume=..., replay=...), each as its own entry point returns it."""
+    cu = _i64(cu_seqlens)
+    B = len(cu) - 1
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    out_dtype = out_dtype or k.dtype
+    keep = []   # host arrays that must outlive the call
+    res = {}
+    pa = ra = ya = None
+    tokens, ranges = 0, 0
+    readout = False
+    if prefill is not None:
+        f = dict(prefill)
+        rd = f.get("readout", True)
+        o = f.get("o") if rd else None
+        if rd and o is None:
+            o = torch.empty((T, H, dv), dtype=out_dtype, device=dev)
+        S_final = f.get("S_final")
+        if S_final is None:
+            S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+        flat, cu_ck = _flatten_ckpts(f.get("ckpt_pos"), B)
+        n_ck = 0 if cu_ck is None else int(cu_ck[-1])
+        ck = f.get("ckpt_states")
+        if ck is None and n_ck > 0:
+            ck = torch.empty((n_ck, H, dv, dk), dtype=torch.float32, device=dev)
+        keep += [flat, cu_ck]
+        pa = _PrefillArgs(_ptr(f.get("S0")), _ptr(o), _ptr(S_final), _p64(flat) if n_ck > 0 else None, _p64(cu_ck),
+                          _ptr(ck))
+        res["prefill"] = {"o": o, "S_final": S_final, "ckpt_states": ck}
+        readout = readout or rd
+        tokens, ranges = tokens + T, ranges + B
+    if resume is not None:
+        f = dict(resume)
+        rd = f.get("readout", True)
+        probes = f["probes"]
+        ckpt_pos = f["ckpt_pos"]
+        flat, cu_ck = _flatten_ckpts(ckpt_pos, B)
+        n_ck = 0 if cu_ck is None else int(cu_ck[-1])
+        P = len(probes)
+        seqs = np.ascontiguousarray(np.asarray([int(s) for s, _ in probes], dtype=np.int32))
+        deps = _i64(int(d) for _, d in probes)
+        chosen = np.zeros(P, dtype=np.int64)
+        offs = np.zeros(P + 1, dtype=np.int64)
+        o_out = f.get("o_out") if rd else None
+        if rd and o_out is None:
+            rows = 0
+            for s, d in probes:
+                lst = list(ckpt_pos[s]) if ckpt_pos is not None else []
+                j = gdn_select_ckpt(lst, int(d))
+                rows += int(d) - (0 if j < 0 else lst[j])
+            o_out = torch.empty((max(rows, 0), H, dv), dtype=out_dtype, device=dev)
+        S_out = f.get("S_out")
+        if S_out is None:
+            S_out = torch.empty((P, H, dv, dk), dtype=torch.float32, device=dev)
+        keep += [flat, cu_ck, seqs, deps, chosen, offs]
+        ra = _ResumeArgs(_ptr(f.get("S0")), _ptr(f["ckpt_states"]), _p64(flat) if n_ck > 0 else None, _p64(cu_ck), P,
+                         seqs.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if P else None,
+                         _p64(deps) if P else None, _ptr(S_out), _ptr(o_out), _p64(chosen) if P else None,
+                         _p64(offs))
+        res["resume"] = {"S_out": S_out, "o": o_out, "chosen": chosen, "offsets": offs}
+        readout = readout or rd
+        tokens, ranges = tokens + (int(deps.sum()) if P else 0), ranges + P
+    if replay is not None:
+        f = dict(replay)
+        rd = f.get("readout", False)
+        mm = _i64(f["m"])
+        S_a = f.get("S_a")
+        _, _, _, _, _, _, S_hat, S_exact, o = _replay_buffers(k, v, B, S_a, rd, out_dtype, f.get("S_hat"),
+                                                              f.get("S_exact"), f.get("o"))
+        a_out = np.zeros(B, dtype=np.int64)
+        k_out = np.zeros(B, dtype=np.int64)
+        keep += [mm, a_out, k_out]
+        ya = _ReplayArgs(_p64(mm), int(f["r_num"]), int(f["r_den"]), _ptr(S_a), _ptr(S_hat),
+                         _ptr(S_exact if S_a is not None else None), _ptr(o), _p64(a_out), _p64(k_out))
+        res["replay"] = {"S_hat": S_hat, "S_exact": S_exact if S_a is not None else None, "o": o, "a": a_out,
+                         "k": k_out}
+        readout = readout or rd
+        twin = 2 if S_a is not None else 1
+        tokens, ranges = tokens + int(mm.sum()) * twin, ranges + B * twin
+    ws = ws if ws is not None else _auto_ws(dev, algo, k, v, tokens, ranges)
+    pr = _problem(cu, H, dk, dv, k.dtype, out_dtype, algo)
+    rc = lib().gdn_step(ctypes.byref(pr), _ptr(q if readout else None), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                        ctypes.byref(pa) if pa is not None else None, ctypes.byref(ra) if ra is not None else None,
+                        ctypes.byref(ya) if ya is not None else None, _ptr(ws), ws.numel(), _stream(stream, dev))
+    _check(rc, "gdn_step")
+    if "resume" in res:
+        r = res["resume"]
+        r["chosen"], r["offsets"] = r["chosen"].tolist(), r["offsets"].tolist()
+    if "replay" in res:
+        r = res["replay"]
+        r["a"], r["k"] = r["a"].tolist(), r["k"].tolist()
+    return res
 
 
 def _replay_buffers(k, v, B, S_a, readout, out_dtype, S_hat, S_exact, o):

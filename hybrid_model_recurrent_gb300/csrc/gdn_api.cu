@@ -216,7 +216,7 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
             HostJob t = jobs[i];
             t.job.s0 = jobs[i].job.s0_twin;
             t.job.s_final = jobs[i].job.s_final_twin;
-            t.job.o_row_begin = -1;
+            t.job.o = nullptr;
             t.job.s0_twin = nullptr;
             t.job.s_final_twin = nullptr;
             jobs.push_back(t);
@@ -269,8 +269,9 @@ gdn_status run_jobs_chunked(const LaunchSpec& L, std::vector<HostJob>& jobs, cud
     if (!L.q && L.k) prm->tm_q = prm->tm_k;
     prm->alpha = L.alpha;
     prm->beta = L.beta;
-    prm->o = L.o;
-    prm->o_vec16 = (L.o && aligned(L.o, 16)) ? 1 : 0;
+    prm->o_vec16 = 1;
+    for (const HostJob& j : jobs)
+        if (j.job.o && !aligned(j.job.o, 16)) prm->o_vec16 = 0;
     prm->ckpt_states = L.ckpt_states;
     prm->status = L.status;
     prm->wait_limit_ns = g_wait_ns.load();
@@ -324,7 +325,6 @@ gdn_status run_jobs(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_
     if (!maps) return GDN_ERR_CUDA;
     prm->alpha = L.alpha;
     prm->beta = L.beta;
-    prm->o = L.o;
     prm->ckpt_states = L.ckpt_states;
     prm->status = L.status;
     prm->wait_limit_ns = g_wait_ns.load();
@@ -428,10 +428,18 @@ GDN_EXPORT gdn_status gdn_read_status(const void* workspace, size_t ws_bytes, gd
 // ---------------------------------------------------------------------------------------
 // prefill with sparse checkpoints
 // ---------------------------------------------------------------------------------------
-GDN_EXPORT gdn_status gdn_prefill_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
-                                       const float* alpha, const float* beta, const float* S0, void* o,
-                                       float* S_final, const int64_t* ckpt_pos, const int64_t* cu_ckpt,
-                                       float* ckpt_states, void* workspace, size_t ws_bytes, gdn_stream_t stream) {
+// Address of output row `row` of a [rows, H, d_v] buffer (nullptr when there is no buffer).
+static void* out_row(void* o, const gdn_problem* p, int64_t row) {
+    if (!o) return nullptr;
+    const size_t es = p->out_dtype == GDN_BF16 ? 2 : 4;
+    return static_cast<unsigned char*>(o) + (size_t)row * (size_t)p->num_heads * (size_t)p->d_v * es;
+}
+
+// Every check of a prefill and its job table, nothing enqueued.
+static gdn_status prefill_prepare(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                  const float* alpha, const float* beta, const float* S0, void* o, float* S_final,
+                                  const int64_t* ckpt_pos, const int64_t* cu_ckpt, float* ckpt_states,
+                                  void* workspace, size_t ws_bytes, std::vector<HostJob>& jobs, LaunchSpec& L) {
     std::vector<int64_t> lens;
     gdn_status st = check_problem(p, lens);
     if (st != GDN_OK) return st;
@@ -453,35 +461,47 @@ GDN_EXPORT gdn_status gdn_prefill_ckpt(const gdn_problem* p, const void* q, cons
         if (n_ck >= ((int64_t)1 << 23)) return GDN_ERR_UNSUPPORTED;
     }
     const size_t D = (size_t)p->num_heads * p->d_v * p->d_k;
-    std::vector<HostJob> jobs(B);
+    jobs.assign(B, HostJob{});
     for (int b = 0; b < B; ++b) {
         gdn::Job& j = jobs[b].job;
         std::memset(&j, 0, sizeof(j));
         j.tok_begin = p->cu_seqlens[b];
         j.len = (int32_t)lens[b];
-        j.o_row_begin = o ? p->cu_seqlens[b] : -1;
+        j.o = out_row(o, p, p->cu_seqlens[b]);
         j.s0 = S0 ? S0 + (size_t)b * D : nullptr;
         j.s_final = S_final + (size_t)b * D;
         if (cu_ckpt)
             for (int64_t i = cu_ckpt[b]; i < cu_ckpt[b + 1]; ++i)
                 jobs[b].ckpts.push_back(gdn::Ckpt{(int32_t)ckpt_pos[i], (int32_t)i});
     }
-    LaunchSpec L{p, q, k, v, alpha, beta, o, ckpt_states, static_cast<unsigned int*>(workspace), o != nullptr, false,
-                 ws_bytes};
-    if ((st = check_two_pass(L, jobs)) != GDN_OK) return st;
+    L = LaunchSpec{p, q, k, v, alpha, beta, o, ckpt_states, static_cast<unsigned int*>(workspace), o != nullptr,
+                   false, ws_bytes};
+    return check_two_pass(L, jobs);
+}
+
+GDN_EXPORT gdn_status gdn_prefill_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                       const float* alpha, const float* beta, const float* S0, void* o,
+                                       float* S_final, const int64_t* ckpt_pos, const int64_t* cu_ckpt,
+                                       float* ckpt_states, void* workspace, size_t ws_bytes, gdn_stream_t stream) {
+    std::vector<HostJob> jobs;
+    LaunchSpec L{};
+    gdn_status st = prefill_prepare(p, q, k, v, alpha, beta, S0, o, S_final, ckpt_pos, cu_ckpt, ckpt_states,
+                                    workspace, ws_bytes, jobs, L);
+    if (st != GDN_OK) return st;
     return run_jobs(L, jobs, (cudaStream_t)stream);
 }
 
 // ---------------------------------------------------------------------------------------
 // resume from the deepest checkpoint at or below d
 // ---------------------------------------------------------------------------------------
-GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
-                                           const float* alpha, const float* beta, const float* S0,
-                                           const float* ckpt_states, const int64_t* ckpt_pos,
-                                           const int64_t* cu_ckpt, int32_t num_probes, const int32_t* probe_seq,
-                                           const int64_t* probe_depth, float* S_out, void* o_out,
-                                           int64_t* chosen_pos, int64_t* o_offsets, void* workspace,
-                                           size_t ws_bytes, gdn_stream_t stream) {
+// Every check of a resume, its index plan (chosen checkpoint and packed output offset per probe) and
+// its job table, nothing enqueued.
+static gdn_status resume_prepare(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                 const float* alpha, const float* beta, const float* S0, const float* ckpt_states,
+                                 const int64_t* ckpt_pos, const int64_t* cu_ckpt, int32_t num_probes,
+                                 const int32_t* probe_seq, const int64_t* probe_depth, float* S_out, void* o_out,
+                                 void* workspace, size_t ws_bytes, std::vector<HostJob>& jobs, LaunchSpec& L,
+                                 std::vector<int64_t>& chosen, std::vector<int64_t>& offs) {
     std::vector<int64_t> lens;
     gdn_status st = check_problem(p, lens);
     if (st != GDN_OK) return st;
@@ -500,8 +520,9 @@ GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, 
             if (!ckpts_valid(ckpt_pos + cu_ckpt[b], cu_ckpt[b + 1] - cu_ckpt[b], lens[b])) return GDN_ERR_INVALID_ARG;
     }
     const size_t D = (size_t)p->num_heads * p->d_v * p->d_k;
-    std::vector<HostJob> jobs(num_probes);
-    std::vector<int64_t> chosen(num_probes), offs(num_probes + 1, 0);
+    jobs.assign(num_probes, HostJob{});
+    chosen.assign(num_probes, 0);
+    offs.assign(num_probes + 1, 0);
     int64_t total = 0;
     for (int32_t i = 0; i < num_probes; ++i) {
         const int s = probe_seq[i];
@@ -520,15 +541,30 @@ GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, 
         std::memset(&jb, 0, sizeof(jb));
         jb.tok_begin = p->cu_seqlens[s] + c;
         jb.len = (int32_t)(d - c);
-        jb.o_row_begin = o_out ? offs[i] : -1;
+        jb.o = out_row(o_out, p, offs[i]);
         jb.s0 = j < 0 ? (S0 ? S0 + (size_t)s * D : nullptr) : ckpt_states + (size_t)(cu_ckpt[s] + j) * D;
         jb.s_final = S_out + (size_t)i * D;
     }
     offs[num_probes] = total;
     if ((st = check_streams(p, q, k, v, alpha, beta, o_out != nullptr, total > 0)) != GDN_OK) return st;
-    LaunchSpec L{p, q, k, v, alpha, beta, o_out, nullptr, static_cast<unsigned int*>(workspace), o_out != nullptr,
-                 false, ws_bytes};
-    if ((st = check_two_pass(L, jobs)) != GDN_OK) return st;
+    L = LaunchSpec{p, q, k, v, alpha, beta, o_out, nullptr, static_cast<unsigned int*>(workspace), o_out != nullptr,
+                   false, ws_bytes};
+    return check_two_pass(L, jobs);
+}
+
+GDN_EXPORT gdn_status gdn_resume_from_ckpt(const gdn_problem* p, const void* q, const void* k, const void* v,
+                                           const float* alpha, const float* beta, const float* S0,
+                                           const float* ckpt_states, const int64_t* ckpt_pos,
+                                           const int64_t* cu_ckpt, int32_t num_probes, const int32_t* probe_seq,
+                                           const int64_t* probe_depth, float* S_out, void* o_out,
+                                           int64_t* chosen_pos, int64_t* o_offsets, void* workspace,
+                                           size_t ws_bytes, gdn_stream_t stream) {
+    std::vector<HostJob> jobs;
+    LaunchSpec L{};
+    std::vector<int64_t> chosen, offs;
+    gdn_status st = resume_prepare(p, q, k, v, alpha, beta, S0, ckpt_states, ckpt_pos, cu_ckpt, num_probes, probe_seq,
+                                   probe_depth, S_out, o_out, workspace, ws_bytes, jobs, L, chosen, offs);
+    if (st != GDN_OK) return st;
     if (chosen_pos) std::copy(chosen.begin(), chosen.end(), chosen_pos);
     if (o_offsets) std::copy(offs.begin(), offs.end(), o_offsets);
     if (num_probes == 0) return GDN_OK;
@@ -564,7 +600,7 @@ static gdn_status replay_prepare(const gdn_problem* p, const void* q, const void
         std::memset(&j, 0, sizeof(j));
         j.tok_begin = p->cu_seqlens[b] + a;
         j.len = (int32_t)kv[b];
-        j.o_row_begin = o ? p->cu_seqlens[b] + a : -1;
+        j.o = out_row(o, p, p->cu_seqlens[b] + a);
         j.s0 = nullptr;
         j.s0_twin = S_a ? S_a + (size_t)b * D : nullptr;
         j.s_final = S_hat + (size_t)b * D;
@@ -671,6 +707,90 @@ GDN_EXPORT gdn_status gdn_tail_replay_overlap(const gdn_problem* p, const void* 
         if (k_out) std::copy(kv.begin(), kv.end(), k_out);
     }
     return st;
+}
+
+// ---------------------------------------------------------------------------------------
+// one serving step: prefills, resumes and tail replays in a single launch
+// ---------------------------------------------------------------------------------------
+static bool ranges_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+    if (!a || !b || a_bytes == 0 || b_bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+GDN_EXPORT gdn_status gdn_step(const gdn_problem* p, const void* q, const void* k, const void* v,
+                               const float* alpha, const float* beta, const gdn_prefill_args* prefill,
+                               const gdn_resume_args* resume, const gdn_replay_args* replay, void* workspace,
+                               size_t ws_bytes, gdn_stream_t stream) {
+    if (!p) return GDN_ERR_INVALID_ARG;
+    std::vector<HostJob> all, part;
+    LaunchSpec L{};
+    gdn_status st = GDN_OK;
+    bool readout = false;
+    float* ckpt_out = nullptr;
+    if (prefill) {
+        if ((st = prefill_prepare(p, q, k, v, alpha, beta, prefill->S0, prefill->o, prefill->S_final,
+                                  prefill->ckpt_pos, prefill->cu_ckpt, prefill->ckpt_states, workspace, ws_bytes,
+                                  part, L)) != GDN_OK)
+            return st;
+        readout = readout || L.readout;
+        ckpt_out = prefill->ckpt_states;
+        all.insert(all.end(), part.begin(), part.end());
+    }
+    std::vector<int64_t> chosen, offs;
+    if (resume) {
+        if ((st = resume_prepare(p, q, k, v, alpha, beta, resume->S0, resume->ckpt_states, resume->ckpt_pos,
+                                 resume->cu_ckpt, resume->num_probes, resume->probe_seq, resume->probe_depth,
+                                 resume->S_out, resume->o_out, workspace, ws_bytes, part, L, chosen, offs)) != GDN_OK)
+            return st;
+        // the resumes read checkpoints that this launch must not be writing
+        if (prefill && prefill->cu_ckpt && resume->cu_ckpt) {
+            const size_t state_bytes = (size_t)p->num_heads * p->d_v * p->d_k * sizeof(float);
+            const int B = p->num_seqs;
+            if (ranges_overlap(prefill->ckpt_states, (size_t)prefill->cu_ckpt[B] * state_bytes,
+                               resume->ckpt_states, (size_t)resume->cu_ckpt[B] * state_bytes))
+                return GDN_ERR_INVALID_ARG;
+        }
+        readout = readout || L.readout;
+        all.insert(all.end(), part.begin(), part.end());
+    }
+    std::vector<int64_t> av, kv;
+    if (replay) {
+        if ((st = plan_all(p->num_seqs, replay->m, replay->r_num, replay->r_den, av, kv)) != GDN_OK) return st;
+        if ((st = replay_prepare(p, q, k, v, alpha, beta, replay->m, kv.data(), replay->S_a, replay->S_hat,
+                                 replay->S_exact, replay->o, workspace, ws_bytes, part, L)) != GDN_OK)
+            return st;
+        readout = readout || L.readout;
+        // the exact twins as jobs of their own: the same tokens from S_a, no readout
+        const size_t n = part.size();
+        for (size_t i = 0; i < n; ++i) {
+            if (!part[i].job.s0_twin) continue;
+            HostJob t = part[i];
+            t.job.s0 = part[i].job.s0_twin;
+            t.job.s_final = part[i].job.s_final_twin;
+            t.job.o = nullptr;
+            t.job.s0_twin = nullptr;
+            t.job.s_final_twin = nullptr;
+            part[i].job.s0_twin = nullptr;
+            part[i].job.s_final_twin = nullptr;
+            part.push_back(t);
+        }
+        all.insert(all.end(), part.begin(), part.end());
+    }
+    if (readout && !q) return GDN_ERR_INVALID_ARG;
+    LaunchSpec M{p, q, k, v, alpha, beta, nullptr, ckpt_out, static_cast<unsigned int*>(workspace), readout, false,
+                 ws_bytes};
+    if ((st = check_two_pass(M, all)) != GDN_OK) return st;
+    if (resume) {
+        if (resume->chosen_pos) std::copy(chosen.begin(), chosen.end(), resume->chosen_pos);
+        if (resume->o_offsets) std::copy(offs.begin(), offs.end(), resume->o_offsets);
+    }
+    if (replay) {
+        if (replay->a_out) std::copy(av.begin(), av.end(), replay->a_out);
+        if (replay->k_out) std::copy(kv.begin(), kv.end(), replay->k_out);
+    }
+    if (all.empty()) return GDN_OK;
+    return run_jobs(M, all, (cudaStream_t)stream);
 }
 
 GDN_EXPORT gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, const int64_t* m,

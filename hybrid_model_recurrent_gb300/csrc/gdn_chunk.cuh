@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_kernel(const __grid_con
     const int64_t tok_begin = job.tok_begin;
     const int len = job.len;
     const int ck_begin = job.ck_begin, ck_end = job.ck_begin + job.ck_count;
-    const int64_t o_row0 = job.o_row_begin;
+    void* const o_job = job.o;
     const uint64_t limit = p.wait_limit_ns;
     const size_t head_state = (size_t)h * D * D;
 
@@ -570,15 +570,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_kernel(const __grid_con
                     for (int nt = 0; nt < 2; ++nt) mma(O[mt][nt], pl, bh[nt][0], bh[nt][1]);
                 }
             }
-            if (o_row0 >= 0) {
-                OutT* obase = reinterpret_cast<OutT*>(p.o) + (size_t)h * D + 16 * warp + 2 * c4;
+            if (o_job != nullptr) {
+                OutT* obase = reinterpret_cast<OutT*>(o_job) + (size_t)h * D + 16 * warp + 2 * c4;
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int t = 16 * mt + g + 8 * hh;
                         if (t < clen) {
-                            OutT* orow = obase + (size_t)(o_row0 + cur.begin + t) * (size_t)H * D;
+                            OutT* orow = obase + (size_t)(cur.begin + t) * (size_t)H * D;
 #pragma unroll
                             for (int nt = 0; nt < 2; ++nt) {
                                 if constexpr (OUT_BF16)

@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
     const int64_t tok_begin = job.tok_begin;
     const int len = job.len;
     const int ck_end = job.ck_begin + job.ck_count;
-    const int64_t o_row0 = job.o_row_begin;
-    const bool rd = READOUT && o_row0 >= 0;
+    void* const o_job = job.o;
+    const bool rd = READOUT && o_job != nullptr;
     const uint64_t limit = p.wait_limit_ns;
     const uint64_t drain_limit = limit > kDrainLimitNs ? limit : kDrainLimitNs;
     const size_t head_state = (size_t)h * D * D;
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
             const float qk0 = R.qk0;
             const size_t tstride = (size_t)H * D;
             const bool vec = p.o_vec16 != 0;
-            OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)(o_row0 + R.begin) * tstride + (size_t)h * D +
+            OutT* ob = reinterpret_cast<OutT*>(o_job) + (size_t)R.begin * tstride + (size_t)h * D +
                        (vec ? 32 * lq : row);
             OutT* stg = reinterpret_cast<OutT*>(smem + OFF_OST + lq * 2048);
             constexpr int kTok = 2048 / (32 * (int)sizeof(OutT));   // tokens per staged tile: 32 bf16, 16 fp32
@@ -894,7 +894,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 const float qk0 = Ro.qk0;
                 const size_t tstride = (size_t)H * D;
                 const bool vec = p.o_vec16 != 0;
-                OutT* ob = reinterpret_cast<OutT*>(p.o) + (size_t)(o_row0 + Ro.begin + t0) * tstride + (size_t)h * D +
+                OutT* ob = reinterpret_cast<OutT*>(o_job) + (size_t)(Ro.begin + t0) * tstride + (size_t)h * D +
                            (vec ? 32 * lq : row);
                 OutT* stg = reinterpret_cast<OutT*>(smem + OFF_OST + pw * 1024);
                 constexpr int kTok = 1024 / (32 * (int)sizeof(OutT));   // tokens per tile: 16 bf16, 8 fp32

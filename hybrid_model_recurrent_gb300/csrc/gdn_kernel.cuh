@@ -58,7 +58,7 @@ enum : unsigned { STATUS_TIMEOUT = 1u };
 // One scan over a contiguous token range, the same for all heads.
 struct Job {
     int64_t tok_begin;      // absolute stream row of the job's first token
-    int64_t o_row_begin;    // absolute output row of the first token; -1: no readout
+    void* o;                // output row of the job's first token ([rows, H, dv]); nullptr: no readout
     const float* s0;        // [H, dv, dk] initial state, nullptr = zeros
     const float* s0_twin;   // [H, dv, dk] initial state of the twin (twin kernels)
     float* s_final;         // [H, dv, dk] state after the last token
@@ -81,7 +81,6 @@ struct Params {
     CUtensorMap tm_v;   // [T, H, dv] box (rows_per_cta, 1, kChunk)
     const float* alpha; // [T, H]
     const float* beta;  // [T, H]
-    void* o;            // [rows, H, dv]
     float* ckpt_states; // [slots, H, dv, dk]
     unsigned int* status;
     unsigned long long wait_limit_ns;
@@ -92,7 +91,7 @@ struct Params {
     int32_t ctas_per_head;  // dv / rows_per_cta
     int32_t n_jobs;
     int32_t stall_after;    // testing hook: stop issuing input copies after this many chunks (-1: off)
-    int32_t o_vec16;        // o is 16-byte aligned: the chunked kernel may write it in 16-byte pieces
+    int32_t o_vec16;        // every job's o is 16-byte aligned: the chunked kernel may write it in 16-byte pieces
     // two-pass chunked path only: the chunk schedule and T = (I + L)^-1 of every chunk, computed by
     // parallel passes before the state scan (workspace buffers)
     CUtensorMap tm_t;       // t_ops as [4 * t_rows, 64] bf16, box (64, 64), 128-byte swizzle
@@ -487,9 +486,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
     }
 
-    const int64_t o_row0 = p.jobs[job_idx].o_row_begin;
-    OutT* const o_base = reinterpret_cast<OutT*>(p.o) + (size_t)h * (size_t)dv + (size_t)(rb * RB + my_row);
-    const bool o_lane = READOUT && o_row0 >= 0 && my_state == 0 && (cl & 1) == 0;
+    void* const o_job = p.jobs[job_idx].o;
+    OutT* const o_base = reinterpret_cast<OutT*>(o_job) + (size_t)h * (size_t)dv + (size_t)(rb * RB + my_row);
+    const bool o_lane = READOUT && o_job != nullptr && my_state == 0 && (cl & 1) == 0;
     for (int tg = 0; ok && tg < len; ++tg) {
         const int c = tg / kChunk;
         const int tau = tg - c * kChunk;
@@ -549,7 +548,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             const float pqr = reduce_slots(pq, lane);
             if (o_lane) {
                 const float ov = sct.x * pqr;
-                OutT* op = o_base + (size_t)(o_row0 + tg) * (size_t)H * (size_t)dv;
+                OutT* op = o_base + (size_t)tg * (size_t)H * (size_t)dv;
                 if constexpr (OUT_BF16)
                     *op = __float2bfloat16_rn(ov);
                 else

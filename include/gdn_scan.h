@@ -206,6 +206,69 @@ gdn_status gdn_tail_replay_k(const gdn_problem* p, const void* q, const void* k,
                              size_t ws_bytes, gdn_stream_t stream);
 
 /*
+ * One serving step's scans in a single launch: the prefills of gdn_prefill_ckpt,
+ * the resumes of gdn_resume_from_ckpt and the tail replays of gdn_tail_replay over
+ * the same packed streams, as one job list ordered longest first.  The short
+ * resume and replay jobs then run on the multiprocessors that the long prefills
+ * leave free, instead of after them.  The setting is the pages' serving step: the
+ * "Sparse prefix caching ..." page (section 3) serves new prompts that store
+ * checkpoints beside requests resumed from checkpoints stored earlier, and the
+ * "Tail-Replay" notes page (section 2.2) recovers the states of cache hits by
+ * replay.
+ *
+ * Each part is optional (NULL skips it) and takes the arguments of its own entry
+ * point, with the same meaning, index plan and checks; every state and output
+ * equals, bit for bit, what that entry point gives for the same part on its own.
+ * The exact twin of a replay (S_a given) runs as jobs of its own.
+ *
+ * The parts of one call run at the same time, so none may read what another
+ * writes: the resumes read checkpoints stored by earlier calls, and
+ * resume->ckpt_states overlapping prefill->ckpt_states is GDN_ERR_INVALID_ARG;
+ * no output may alias an input or another output (not checked).  q may be NULL
+ * only when no part has a readout.  The per-part host outputs (chosen_pos,
+ * o_offsets, a_out, k_out) are written once every check has passed.
+ */
+typedef struct gdn_prefill_args {
+    const float* S0;            /* as gdn_prefill_ckpt                              */
+    void* o;
+    float* S_final;
+    const int64_t* ckpt_pos;
+    const int64_t* cu_ckpt;
+    float* ckpt_states;         /* written by this call                             */
+} gdn_prefill_args;
+
+typedef struct gdn_resume_args {
+    const float* S0;            /* as gdn_resume_from_ckpt                          */
+    const float* ckpt_states;   /* read by this call: stored by an earlier one      */
+    const int64_t* ckpt_pos;
+    const int64_t* cu_ckpt;
+    int32_t num_probes;
+    const int32_t* probe_seq;
+    const int64_t* probe_depth;
+    float* S_out;
+    void* o_out;
+    int64_t* chosen_pos;
+    int64_t* o_offsets;
+} gdn_resume_args;
+
+typedef struct gdn_replay_args {
+    const int64_t* m;           /* as gdn_tail_replay                               */
+    int32_t r_num;
+    int32_t r_den;
+    const float* S_a;
+    float* S_hat;
+    float* S_exact;
+    void* o;
+    int64_t* a_out;
+    int64_t* k_out;
+} gdn_replay_args;
+
+gdn_status gdn_step(const gdn_problem* p, const void* q, const void* k, const void* v,
+                    const float* alpha, const float* beta, const gdn_prefill_args* prefill,
+                    const gdn_resume_args* resume, const gdn_replay_args* replay, void* workspace,
+                    size_t ws_bytes, gdn_stream_t stream);
+
+/*
  * Tail replay with the prefix's cached attention KV copied to the device at the
  * same time ("Tail-Replay" notes page, section 2.5, transfer / replay overlap:
  * the replay needs only the tail's inputs, not the KV, so the two run on

@@ -192,3 +192,44 @@ def test_resume_and_replay_reject_bad_arguments(L):
     assert replay([10, 5], rd=0) == E
     assert replay([10, 5], S_a=_vp(0xb000)) == E               # S_a without S_exact
     assert replay([10, 5], S_hat=None) == E
+
+
+def test_step_rejects_bad_arguments_and_writes_no_host_output(L):
+    pr, _keep = _prob()
+    P64, P32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+    E = gdn.GDN_ERR_INVALID_ARG
+    pos, cu = _p64([4, 8, 20]), _p64([0, 2, 3])
+    seqs = np.ascontiguousarray(np.asarray([0, 1], dtype=np.int32))
+    deps = _p64([9, 15])
+    mm = _p64([10, 20])
+
+    def call(pf=True, rs=True, rp=True, q=_vp(0), resume_ck=_vp(0x20000), prefill_ck=_vp(0x7000), rs_readout=True,
+             m=None):
+        chosen = np.full(2, -7, dtype=np.int64)
+        a_out = np.full(2, -7, dtype=np.int64)
+        pa = gdn._PrefillArgs(None, _vp(0x5000), _vp(0x6000), pos.ctypes.data_as(P64), cu.ctypes.data_as(P64),
+                              prefill_ck)
+        ra = gdn._ResumeArgs(None, resume_ck, pos.ctypes.data_as(P64), cu.ctypes.data_as(P64), 2,
+                             seqs.ctypes.data_as(P32), deps.ctypes.data_as(P64), _vp(0x9000),
+                             _vp(0x30000) if rs_readout else None, chosen.ctypes.data_as(P64), None)
+        m_arr = mm if m is None else _p64(m)
+        ya = gdn._ReplayArgs(m_arr.ctypes.data_as(P64), 1, 20, None, _vp(0xa000), None, None,
+                             a_out.ctypes.data_as(P64), None)
+        rc = L.gdn_step(ctypes.byref(pr), q, _vp(0x1000), _vp(0x2000), _vp(0x3000), _vp(0x4000),
+                        ctypes.byref(pa) if pf else None, ctypes.byref(ra) if rs else None,
+                        ctypes.byref(ya) if rp else None, _vp(0x8000), 256, None)
+        return rc, chosen, a_out
+
+    # the resumes may not read checkpoints that the same call's prefill writes (3 slots x 2 heads x 32 x 32 fp32)
+    for ck in (_vp(0x7000), _vp(0x7000 + 3 * 2 * 32 * 32 * 4 - 16), _vp(0x7000 - 3 * 2 * 32 * 32 * 4 + 16)):
+        rc, chosen, a_out = call(resume_ck=ck)
+        assert rc == E and (chosen == -7).all() and (a_out == -7).all()
+    assert call(resume_ck=_vp(0x7000 + 3 * 2 * 32 * 32 * 4), q=None)[0] == E   # readouts without q
+    assert call(rs=False, rp=False, q=None)[0] == E                               # the prefill's readout needs q
+    rc, chosen, a_out = call(m=[11, 5])                                            # m > N: every part checked first
+    assert rc == E and (chosen == -7).all() and (a_out == -7).all()
+    import torch
+    if not torch.cuda.is_available():
+        # valid calls (fake pointers): the library gets as far as CUDA, which is absent here
+        assert call(resume_ck=_vp(0x7000 + 3 * 2 * 32 * 32 * 4))[0] == gdn.GDN_ERR_CUDA
+        assert call(pf=False, rp=False, rs_readout=False, q=None, resume_ck=_vp(0x7000))[0] == gdn.GDN_ERR_CUDA
