@@ -362,24 +362,22 @@ def two_pass_report(step, reps: int = 5):
     return out
 
 
-def step_forms_report(step, reps: int = 20):
-    """The timed step as one gdn_step launch against the three entry points one after another (medians of
-    CUDA-event spans over one step each)."""
+def step_forms_report(step, reps: int = 50):
+    """The timed step as one gdn_step launch against the three entry points one after another: CUDA events
+    around `reps` back-to-back steps (the device stays busy, so host time between calls is hidden), per step."""
     dev = step.dev
     out = {}
     for name, fn in (("one_launch_ms", step.run), ("three_calls_ms", step.run_three_calls)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize(dev)
-        ts = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
         for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
             fn()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            ts.append(e0.elapsed_time(e1))
-        out[name] = float(np.median(ts))
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out[name] = e0.elapsed_time(e1) / reps
     out["note"] = ("one launch: the prefill's 128 (sequence, head) jobs take 128 of the 152 SMs and the short "
                    "resume and replay jobs run on the other 24 during it")
     return out
@@ -438,6 +436,107 @@ def overlap_report(dev, reps: int = 5):
             "model_max": max(t_rep, t_kv), "model_sum": t_rep + t_kv,
             "kv_GBps": kv_bytes / (t_kv * 1e-3) / 1e9,
             "replay_Mtok_head_per_s": k_tail * H / (t_rep * 1e-3) / 1e6}
+
+
+def workloads_report(dev, hbm_peak: float, reps: int = 5):
+    """Every synthetic workload on its own (CUDA events around `reps` back-to-back calls, per call).
+    Throughput in tok*head/s and, against the HBM peak, the algorithmic bytes of the call: per tok*head
+    q, k, v + gates + o (1,032 B at bf16 d = 128) with a readout, k, v + gates (520 B) without; 64 KiB per
+    state read or written.  The replay workloads are given as their tails alone (the rows the kernel reads:
+    a sequence of k_b rows replayed whole), which is the same scan over the same tokens as ceil(r m_b) of a
+    prefix of m_b."""
+    import hybrid_model_recurrent_gb300 as gdn
+    ws = gdn.workspace(dev)
+    out = {}
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    def row(ms, tok_head, nbytes, states=None):
+        r = {"ms": ms, "tok_head": tok_head, "Mtok_head_per_s": tok_head / (ms * 1e-3) / 1e6,
+             "algorithmic_bytes": nbytes, "achieved_GBps": nbytes / (ms * 1e-3) / 1e9,
+             "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_peak}
+        if states is not None:
+            r["states_per_s"] = states / (ms * 1e-3)
+        return r
+
+    def per_tok(w, readout):
+        es = 2 if w.qkv_dtype == torch.bfloat16 else 4
+        eo = 2 if w.out_dtype == torch.bfloat16 else 4
+        return (w.dk + w.dv + (w.dk if readout else 0)) * es + 8 + (w.dv * eo if readout else 0)
+
+    # tiny: prefill (readout, checkpoints every 64), 4 resume probes, tail replay r = 1/20 at m = 256 with twin
+    w = synth.workload("tiny")
+    x = synth.make_inputs(w, device=dev)
+    cu, ck, D = w.cu_seqlens, w.ckpt_positions(), w.dv * w.dk * 4
+    r = gdn.gdn_prefill_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, ckpt_pos=ck, ws=ws)
+    probes = [(0, 100), (0, 191), (0, 200), (0, 256)]
+    S_a = torch.zeros((1, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    t_pf = timed(lambda: gdn.gdn_prefill_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, ckpt_pos=ck, ws=ws))
+    t_rs = timed(lambda: gdn.gdn_resume_from_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, r["ckpt_states"], ck, probes,
+                                                  ws=ws))
+    t_rp = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, [256], 1, 20, S_a=S_a, ws=ws))
+    n_rs = sum(d - max([c for c in ck[0] if c <= d], default=0) for _, d in probes)
+    out["tiny"] = {"prefill": row(t_pf, 256 * w.H, 256 * w.H * per_tok(w, True) + w.H * 5 * D, 4 * w.H),
+                   "resume": row(t_rs, n_rs * w.H, n_rs * w.H * per_tok(w, True) + len(probes) * w.H * 2 * D),
+                   "replay_with_twin": row(t_rp, 13 * w.H, 13 * w.H * per_tok(w, False) + w.H * 3 * D),
+                   "note": "d = 32 fp32 (per-token kernel); launch-bound"}
+    del x, r
+
+    # long prefill: 4 x 32 heads, N = 131072, 32 checkpoints; then the 64 resume probes
+    w = synth.workload("long")
+    x = synth.make_inputs(w, device=dev)
+    cu, ck, D = w.cu_seqlens, w.ckpt_positions(), w.dv * w.dk * 4
+    o = torch.empty((w.T, w.H, w.dv), dtype=w.out_dtype, device=dev)
+    S_f = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    cks = torch.empty((sum(len(c) for c in ck), w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    t_pf = timed(lambda: gdn.gdn_prefill_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, ckpt_pos=ck, o=o, S_final=S_f,
+                                              ckpt_states=cks, ws=ws))
+    probes = w.probes()
+    n_rs = sum(d - max([c for c in ck[s] if c <= d], default=0) for s, d in probes)
+    o_r = torch.empty((max(n_rs, 1), w.H, w.dv), dtype=w.out_dtype, device=dev)
+    S_o = torch.empty((len(probes), w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    t_rs = timed(lambda: gdn.gdn_resume_from_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, cks, ck, probes, o_out=o_r,
+                                                  S_out=S_o, ws=ws))
+    n_ck = cks.shape[0] * w.H
+    out["long"] = {"prefill": row(t_pf, w.T * w.H, w.T * w.H * per_tok(w, True) + (n_ck + w.B * w.H) * D, n_ck),
+                   "resume": row(t_rs, n_rs * w.H, n_rs * w.H * per_tok(w, True) + len(probes) * w.H * 2 * D),
+                   "note": "prefill: 128 (sequence, head) scans of 131072 tokens; resume: 64 probes x 32 heads"}
+    del x, o, S_f, cks, o_r, S_o
+    torch.cuda.empty_cache()
+
+    # tail replays: 768 scans x 1639 (5 % of 32768), with and without the exact twin; 32 ragged requests x
+    # 16 heads, k_b = ceil(m_b / 10)
+    for name in ("replay5", "ragged10"):
+        wf = synth.workload(name)
+        rn, rd = wf.replay_r
+        tails = [gdn.gdn_replay_plan(m, rn, rd)[1] for m in wf.seq_lens]
+        w = synth.Workload(name + "-tails", tails, wf.H, wf.dk, wf.dv, wf.qkv_dtype, wf.out_dtype, wf.alpha_lo,
+                           wf.alpha_hi, wf.beta_kind, seed=wf.seed)
+        x = synth.make_inputs(w, device=dev, with_q=False)
+        cu, D = w.cu_seqlens, w.dv * w.dk * 4
+        S_h = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+        t = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, tails, 1, 1, S_hat=S_h, ws=ws))
+        rows = {"replay": row(t, w.T * w.H, w.T * w.H * per_tok(w, False) + w.B * w.H * D)}
+        if name == "replay5":
+            S_a = synth.state(101, w.B * w.H, w.dv, w.dk, 1.0, device=dev).view(w.B, w.H, w.dv, w.dk)
+            S_e = torch.empty_like(S_h)
+            t2 = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, tails, 1, 1, S_a=S_a,
+                                                   S_hat=S_h, S_exact=S_e, ws=ws))
+            rows["replay_with_twin"] = row(t2, 2 * w.T * w.H, w.T * w.H * per_tok(w, False) + w.B * w.H * 3 * D)
+        rows["note"] = f"{w.B * w.H} scans, {w.T * w.H} tail tok*head"
+        out[name] = rows
+        del x, S_h
+        torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline(w: synth.Workload):
@@ -661,6 +760,7 @@ def run_ours(args, ws, rank, local):
             "replay_overlap": overlap_report(dev),
             "chunked_variants": two_pass_report(step),
             "step_forms": step_forms_report(step),
+            "workloads": workloads_report(dev, hbm_peak),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
