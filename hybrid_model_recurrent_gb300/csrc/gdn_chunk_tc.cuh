@@ -96,9 +96,9 @@ constexpr int OFF_WL = 147456;         //   lo
 constexpr int OFF_UH = 163840;         // [128 dv][64 t] U''^T hi (K-major A operand)
 constexpr int OFF_UL = 180224;         //   lo
 constexpr int OFF_LF = 196608;         // fp32 [64][68]: L, then T in place
-constexpr int OFF_LD = 214016;         // fp32 4 x [16][17] diagonal blocks of L; later [32][33] scratch
-constexpr int OFF_PSC = 218368;        // fp32 prep scalars [2][4][64]: gamma, 1/gamma, beta gamma, beta
-constexpr int OFF_RING = 220416;       // Ring[kRing]
+constexpr int OFF_LD = 214016;         // fp32 4 x [16][17] diagonal blocks of L; later [32][kLdY] scratch
+constexpr int OFF_PSC = 218624;        // fp32 prep scalars [2][4][64]: gamma, 1/gamma, beta gamma, beta
+constexpr int OFF_RING = 220672;       // Ring[kRing]
 constexpr int OFF_BAR = OFF_RING + kRing * 576;
 constexpr int kBarBytes = 256;
 constexpr int OFF_OST = OFF_BAR + kBarBytes;   // 8 KB: readout staging, a [tokens][32 rows] tile per reading warp
@@ -107,6 +107,12 @@ static_assert(OFF_U0 + 2 * 128 * 4 <= OFF_LD, "u_1 buffer inside the L area");
 constexpr int kSmemBytes = OFF_OST + 4 * 2048 + 1024;
 static_assert(kSmemBytes <= 232448, "227 KB of shared memory per block");
 constexpr int kLdF = 68;
+// Row strides of the merge scratch, chosen so that the mma.sync fragments (rows g8 and 2 t4, 2 t4 + 1) and the
+// float pairs written back fall in distinct banks: level B [32][36] in the L area, level A [16][20] in a warp's
+// two spent diagonal blocks of L.
+constexpr int kLdY = 36, kLdS = 20;
+static_assert(OFF_LD + 32 * kLdY * 4 <= OFF_PSC, "level-B scratch inside the L area");
+static_assert(16 * kLdS <= 2 * 16 * 17, "level-A scratch inside two diagonal blocks");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(OFF_PSC + 2 * 4 * C * 4 == OFF_RING, "scalar area");
 
@@ -302,11 +308,17 @@ __device__ __forceinline__ int gamma_first(float g0, float g1) {
 // accumulate): half the instructions of the tf32 form for the same K; the caller adds c to d at the end
 __device__ __forceinline__ void mma_bf16x3(float (&d)[4], float (&c)[4], const float* a, int lda, const float* b,
                                            int ldb, int g8, int t4) {
+    // A pairs as 8-byte loads (a and lda even at every call): with lda = 68 the 32 lanes' pairs fill each bank
+    // exactly twice, the minimum for 256 bytes
     uint32_t ah[4], al[4], bh[2], bl[2];
-    split_pair(a[g8 * lda + 2 * t4], a[g8 * lda + 2 * t4 + 1], ah[0], al[0]);
-    split_pair(a[(g8 + 8) * lda + 2 * t4], a[(g8 + 8) * lda + 2 * t4 + 1], ah[1], al[1]);
-    split_pair(a[g8 * lda + 2 * t4 + 8], a[g8 * lda + 2 * t4 + 9], ah[2], al[2]);
-    split_pair(a[(g8 + 8) * lda + 2 * t4 + 8], a[(g8 + 8) * lda + 2 * t4 + 9], ah[3], al[3]);
+    const float2 a0 = *reinterpret_cast<const float2*>(a + g8 * lda + 2 * t4);
+    const float2 a1 = *reinterpret_cast<const float2*>(a + (g8 + 8) * lda + 2 * t4);
+    const float2 a2 = *reinterpret_cast<const float2*>(a + g8 * lda + 2 * t4 + 8);
+    const float2 a3 = *reinterpret_cast<const float2*>(a + (g8 + 8) * lda + 2 * t4 + 8);
+    split_pair(a0.x, a0.y, ah[0], al[0]);
+    split_pair(a1.x, a1.y, ah[1], al[1]);
+    split_pair(a2.x, a2.y, ah[2], al[2]);
+    split_pair(a3.x, a3.y, ah[3], al[3]);
     split_pair(b[(2 * t4) * ldb + g8], b[(2 * t4 + 1) * ldb + g8], bh[0], bl[0]);
     split_pair(b[(2 * t4 + 8) * ldb + g8], b[(2 * t4 + 9) * ldb + g8], bh[1], bl[1]);
     mma_bf16_16816(c, al, bh[0], bh[1]);
@@ -1122,10 +1134,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         }
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
-                            sc[g8 * 16 + 8 * nt + 2 * t4] = y[nt][0] + yc[nt][0];
-                            sc[g8 * 16 + 8 * nt + 2 * t4 + 1] = y[nt][1] + yc[nt][1];
-                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4] = y[nt][2] + yc[nt][2];
-                            sc[(g8 + 8) * 16 + 8 * nt + 2 * t4 + 1] = y[nt][3] + yc[nt][3];
+                            sc[g8 * kLdS + 8 * nt + 2 * t4] = y[nt][0] + yc[nt][0];
+                            sc[g8 * kLdS + 8 * nt + 2 * t4 + 1] = y[nt][1] + yc[nt][1];
+                            sc[(g8 + 8) * kLdS + 8 * nt + 2 * t4] = y[nt][2] + yc[nt][2];
+                            sc[(g8 + 8) * kLdS + 8 * nt + 2 * t4 + 1] = y[nt][3] + yc[nt][3];
                         }
                         __syncwarp();
                         float x[2][4], xc[2][4];
@@ -1133,7 +1145,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                             for (int e = 0; e < 4; ++e) x[nt][e] = xc[nt][e] = 0.f;
-                            mma_bf16x3(x[nt], xc[nt], Lf + (16 * ib) * kLdF + 16 * ib, kLdF, sc + 8 * nt, 16, g8, t4);
+                            mma_bf16x3(x[nt], xc[nt], Lf + (16 * ib) * kLdF + 16 * ib, kLdF, sc + 8 * nt, kLdS, g8, t4);
                         }
                         float* dst = Lf + (16 * ib) * kLdF + 16 * jb;
 #pragma unroll
@@ -1183,16 +1195,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                                g8, t4);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) y[e] += yc[e];
-                // L_BA T_AA as [32][33] scratch
-                Yb[(16 * mt + g8) * 33 + 8 * nt + 2 * t4] = y[0];
-                Yb[(16 * mt + g8) * 33 + 8 * nt + 2 * t4 + 1] = y[1];
-                Yb[(16 * mt + g8 + 8) * 33 + 8 * nt + 2 * t4] = y[2];
-                Yb[(16 * mt + g8 + 8) * 33 + 8 * nt + 2 * t4 + 1] = y[3];
+                // L_BA T_AA as [32][kLdY] scratch
+                Yb[(16 * mt + g8) * kLdY + 8 * nt + 2 * t4] = y[0];
+                Yb[(16 * mt + g8) * kLdY + 8 * nt + 2 * t4 + 1] = y[1];
+                Yb[(16 * mt + g8 + 8) * kLdY + 8 * nt + 2 * t4] = y[2];
+                Yb[(16 * mt + g8 + 8) * kLdY + 8 * nt + 2 * t4 + 1] = y[3];
                 group_sync(BAR_PREP, NPREP);
                 float x[4] = {0.f, 0.f, 0.f, 0.f}, xc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks)
-                    mma_bf16x3(x, xc, Lf + (32 + 16 * mt) * kLdF + 32 + 16 * ks, kLdF, Yb + (16 * ks) * 33 + 8 * nt, 33,
+                    mma_bf16x3(x, xc, Lf + (32 + 16 * mt) * kLdF + 32 + 16 * ks, kLdF, Yb + (16 * ks) * kLdY + 8 * nt, kLdY,
                                g8, t4);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) x[e] += xc[e];
