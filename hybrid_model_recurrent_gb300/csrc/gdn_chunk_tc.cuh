@@ -717,9 +717,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= c[i];
-                    st_split32(smem + OFF_UH, smem + OFF_UL, row, 32 * cb, v);
+                    // U''^T as the products' A operand in TMEM, bf16 pairs: hi over the U columns, lo over the W
+                    // columns, each into the 16 columns this thread has just read (block cb = 0) or read before
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) split_pair(v[2 * e], v[2 * e + 1], hw[e], lw[e]);
+                    tmem_st16(trow + T_U + 16 * cb, hw);
+                    tmem_st16(trow + TW + 16 * cb, lw);
                 }
-                proxy_fence();
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar_ufree);
                 // ---- after St += U''^T K: checkpoint / end / small scale -> fold sigma into St ----
@@ -1303,7 +1309,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     sp = 1;
                     progressed = true;
                 }
-                if (sp == 1 && mbar_test(bar_wuin, jp & 1) && (jp == 0 || mbar_test(bar_ufree, (jp - 1) & 1))) {
+                // the U and W columns hold the previous chunk's U'' until its last product (U''^T P^T with a
+                // readout, else the state update) is done
+                if (sp == 1 && mbar_test(bar_wuin, jp & 1) &&
+                    (jp == 0 || mbar_test(rd ? bar_o : bar_st, (jp - 1) & 1))) {
                     tc_fence_after();
                     // W^T = K^T T1^T, U~^T = V^T T2^T
                     const uint32_t inV = sbase + OFF_V;
@@ -1369,11 +1378,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         // St += U''^T K
 #pragma unroll
                         for (int kt = 0; kt < 4; ++kt) {
-                            const uint64_t auh = sdesc(sbase + OFF_UH + kt * 32, 16, 1024);
-                            const uint64_t aul = sdesc(sbase + OFF_UL + kt * 32, 16, 1024);
                             const uint64_t bk = sdesc(inKQ + kt * 2048, 16384, 1024);   // K: MN-major over d_k
-                            umma_ss(tbase + T_S, auh, bk, id128b, 1);
-                            umma_ss(tbase + T_S, aul, bk, id128b, 1);
+                            umma_ts(tbase + T_S, tbase + T_U + 8 * kt, bk, id128b, 1);   // U'' hi
+                            umma_ts(tbase + T_S, tbase + TW + 8 * kt, bk, id128b, 1);    // U'' lo
                         }
                         umma_commit(bar_st);
                         ++cnt[5];
@@ -1388,13 +1395,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                             // O^T += U''^T P^T
 #pragma unroll
                             for (int kt = 0; kt < 4; ++kt) {
-                                const uint64_t auh = sdesc(sbase + OFF_UH + kt * 32, 16, 1024);
-                                const uint64_t aul = sdesc(sbase + OFF_UL + kt * 32, 16, 1024);
                                 const uint64_t bph = sdesc(sbase + OFF_PH + kt * 32, 16, 1024);
                                 const uint64_t bpl = sdesc(sbase + OFF_PL + kt * 32, 16, 1024);
-                                umma_ss(tbase + TO, auh, bph, id64, 1);
-                                umma_ss(tbase + TO, auh, bpl, id64, 1);
-                                umma_ss(tbase + TO, aul, bph, id64, 1);
+                                umma_ts(tbase + TO, tbase + T_U + 8 * kt, bph, id64, 1);
+                                umma_ts(tbase + TO, tbase + T_U + 8 * kt, bpl, id64, 1);
+                                umma_ts(tbase + TO, tbase + TW + 8 * kt, bph, id64, 1);
                             }
                         }
                         umma_commit(bar_o);
