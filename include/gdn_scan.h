@@ -219,7 +219,10 @@ gdn_status gdn_tail_replay_k(const gdn_problem* p, const void* q, const void* k,
  * Each part is optional (NULL skips it) and takes the arguments of its own entry
  * point, with the same meaning, index plan and checks; every state and output
  * equals, bit for bit, what that entry point gives for the same part on its own.
- * The exact twin of a replay (S_a given) runs as jobs of its own.
+ * The exact twin of a replay (S_a given) runs as jobs of its own; on the
+ * token-by-token kernel (sizes other than d_k = d_v = 128 with bf16 q/k/v), whose
+ * replay entry point runs the twin beside the replay in one block, S_exact then
+ * agrees with it to rounding rather than bit for bit.
  *
  * The parts of one call run at the same time, so none may read what another
  * writes: the resumes read checkpoints stored by earlier calls, and
