@@ -332,6 +332,32 @@ def test_identity_gates_leave_state_unchanged(algo):
 
 
 @pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma", "two_pass"])
+def test_row_permutation_equivariance(algo):
+    """Row i of the state evolves from component i of v alone (the key operator acts from the right), so
+    permuting the components of v (and the rows of S0) permutes the rows of every state and the components of
+    every output, whatever the chunking, rounding order or kernel: the GPU results must agree bit for bit."""
+    lens = [200, 75]
+    H, dk, dv = 2, 128, 128
+    w, inp = _inputs(43, lens, H, dk, dv, torch.bfloat16, 0.9, 1.0, beta="sigmoid")
+    cu = w.cu_seqlens
+    ck = [[64, 150], [75]]
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(dv))
+    S0 = synth.state(19, w.B * H, dv, dk, 0.5).view(w.B, H, dv, dk)
+    d = _dev(inp)
+    vp = d.v[:, :, perm.to(DEV)].contiguous()
+    S0p = S0[:, :, perm, :].contiguous()
+    a = gdn.gdn_prefill_ckpt(d.q, d.k, d.v, d.alpha, d.beta, cu, S0=S0.to(DEV), ckpt_pos=ck,
+                             out_dtype=torch.float32, algo=algo)
+    b = gdn.gdn_prefill_ckpt(d.q, d.k, vp, d.alpha, d.beta, cu, S0=S0p.to(DEV), ckpt_pos=ck,
+                             out_dtype=torch.float32, algo=algo)
+    torch.cuda.synchronize()
+    pd = perm.to(DEV)
+    assert torch.equal(b["S_final"], a["S_final"][:, :, pd, :]), "final states: rows permuted"
+    assert torch.equal(b["ckpt_states"], a["ckpt_states"][:, :, pd, :]), "checkpoints: rows permuted"
+    assert torch.equal(b["o"], a["o"][:, :, pd]), "outputs: components permuted"
+
+
+@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma", "two_pass"])
 def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic(algo):
     """Resume from the deepest stored checkpoint c_j <= d reproduces, bit for bit,
     the state at d of a full run that stores the same checkpoints plus d.  (Each
