@@ -129,3 +129,44 @@ def test_step_refuses_resumes_from_checkpoints_it_writes():
                      prefill=dict(ckpt_pos=[[64, 128]], ckpt_states=ck),
                      resume=dict(ckpt_states=ck, ckpt_pos=[[64, 128]], probes=[(0, 100)]))
     assert e.value.status == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_step_at_full_size_in_the_benchmark_configuration():
+    """The benchmark's step: 8 x 16 heads x 8192 tokens, 16 checkpoints, 16 resume probes from a store an
+    earlier prefill wrote, 5 % tail replays, as one launch.  Bit for bit the three entry points' results, and
+    sampled (sequence, head) streams against the oracle."""
+    import dataclasses
+    w = synth.workload("prefill")
+    x = synth.make_inputs(w, device=DEV)
+    cu, ck = w.cu_seqlens, w.ckpt_positions()
+    probes = dataclasses.replace(w, n_probes=16).probes()
+    m = list(w.seq_lens)
+    ws = gdn.workspace(DEV)
+    store = gdn.gdn_prefill_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, ckpt_pos=ck, ws=ws)["ckpt_states"]
+    st = gdn.gdn_step(x.q, x.k, x.v, x.alpha, x.beta, cu, ws=ws, prefill=dict(ckpt_pos=ck),
+                      resume=dict(ckpt_states=store, ckpt_pos=ck, probes=probes),
+                      replay=dict(m=m, r_num=1, r_den=20))
+    pf = gdn.gdn_prefill_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, ckpt_pos=ck, ws=ws)
+    rs = gdn.gdn_resume_from_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, store, ck, probes, ws=ws)
+    rp = gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, m, 1, 20, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(st["prefill"]["o"], pf["o"]) and torch.equal(st["prefill"]["S_final"], pf["S_final"])
+    assert torch.equal(st["prefill"]["ckpt_states"], pf["ckpt_states"])
+    assert torch.equal(st["prefill"]["ckpt_states"], store), "the store and the step's own dumps agree"
+    assert st["resume"]["chosen"] == rs["chosen"] and st["resume"]["offsets"] == rs["offsets"]
+    assert torch.equal(st["resume"]["S_out"], rs["S_out"]) and torch.equal(st["resume"]["o"], rs["o"])
+    assert st["replay"]["k"] == rp["k"] == [410] * w.B and torch.equal(st["replay"]["S_hat"], rp["S_hat"])
+    # sampled streams against the oracle (its checkpoints its own)
+    for i, h in ((0, 5), (7, 11)):
+        s, d = probes[i]
+        sl = slice(cu[s], cu[s + 1])
+        args = (x.q[sl, h].cpu(), x.k[sl, h].cpu(), x.v[sl, h].cpu(), x.alpha[sl, h].cpu(), x.beta[sl, h].cpu())
+        ref = oracle.prefill(*args, ckpt_pos=ck[s], want_o=False)
+        res = oracle.resume(*args, list(ref["ckpt"]), ck[s], d)
+        assert st["resume"]["chosen"][i] == res["c"]
+        assert_close(st["resume"]["S_out"][i, h], res["S"], f"step resume probe {i} h={h}")
+        lo, hi = st["resume"]["offsets"][i], st["resume"]["offsets"][i + 1]
+        if hi > lo:
+            check_output(st["resume"]["o"][lo:hi, h], res["o"], f"step resume o probe {i} h={h}")
+        rep = oracle.tail_replay(args[1], args[2], args[3], args[4], m[s], 1, 20)
+        assert_close(st["replay"]["S_hat"][s, h], rep["S_hat"], f"step replay s={s} h={h}")
