@@ -333,10 +333,11 @@ def placement_report(N: int = 8192, M: int = 16, n_requests: int = 10000):
     return out
 
 
-def two_pass_report(step, reps: int = 5):
+def two_pass_report(step, reps: int = 20):
     """The prefill call of the timed step in both chunked variants, on the step's own inputs: the fused
     tcgen05 scan (the default, 256-byte workspace) and the two-pass scan (chunk schedule and T of every chunk
-    first, then the scan; it needs gdn_workspace_size_two_pass bytes).  Medians of CUDA-event spans."""
+    first, then the scan; it needs gdn_workspace_size_two_pass bytes).  CUDA events around `reps` back-to-back
+    calls, per call."""
     import hybrid_model_recurrent_gb300 as gdn
     w, inp, dev = step.w, step.inp, step.dev
     big = torch.zeros(int(gdn.lib().gdn_workspace_size_two_pass(w.T, w.H, w.B)), dtype=torch.uint8, device=dev)
@@ -348,15 +349,13 @@ def two_pass_report(step, reps: int = 5):
         for _ in range(2):
             call()
         torch.cuda.synchronize(dev)
-        ts = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
         for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
             call()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            ts.append(e0.elapsed_time(e1))
-        out[name] = float(np.median(ts))
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out[name] = e0.elapsed_time(e1) / reps
     out["two_pass_workspace_bytes"] = int(big.numel())
     out["workload"] = "the timed step's prefill call (8 x 16 heads, N = 8192, 16 checkpoints)"
     return out
