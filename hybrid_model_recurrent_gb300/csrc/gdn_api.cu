@@ -712,6 +712,49 @@ GDN_EXPORT gdn_status gdn_tail_replay_overlap(const gdn_problem* p, const void* 
 // ---------------------------------------------------------------------------------------
 // one serving step: prefills, resumes and tail replays in a single launch
 // ---------------------------------------------------------------------------------------
+// Two launch lanes per device for gdn_step: streams of the library's own, the long jobs' of the highest and the
+// short jobs' of the lowest priority (so that the long jobs' CTAs are placed first whatever the order in which
+// the two launches become ready), and the events that fork them from the caller's stream and join them back to
+// it; made on the first call that needs them.
+struct SideLane {
+    cudaStream_t hi = nullptr, lo = nullptr;
+    cudaEvent_t fork = nullptr, join_hi = nullptr, join_lo = nullptr;
+    int sms = 0;
+    bool ready = false;
+};
+static std::mutex g_side_mutex;
+static SideLane g_side[gdn::kMaxOptinDevices];
+
+static SideLane* side_lane() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= gdn::kMaxOptinDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideLane& L = g_side[dev];
+    if (!L.ready) {
+        if (!L.sms && cudaDeviceGetAttribute(&L.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+        if (!L.hi && cudaStreamCreateWithPriority(&L.hi, cudaStreamNonBlocking, greatest) != cudaSuccess)
+            return nullptr;
+        if (!L.lo && cudaStreamCreateWithPriority(&L.lo, cudaStreamNonBlocking, least) != cudaSuccess) return nullptr;
+        for (cudaEvent_t* e : {&L.fork, &L.join_hi, &L.join_lo})
+            if (!*e && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        L.ready = true;
+    }
+    return &L;
+}
+
+// Jobs sorted longest first split into a head of long jobs whose CTAs (one per job and head) all fit on the
+// SMs together and a tail of jobs at most a quarter of the previous one's length; 0 when there is no such split.
+static size_t split_point(const std::vector<HostJob>& jobs, int64_t heads, int sms) {
+    for (size_t b = 1; b < jobs.size(); ++b) {
+        if ((int64_t)b * heads > sms) return 0;
+        if ((int64_t)jobs[b].job.len * 4 <= (int64_t)jobs[b - 1].job.len) return b;
+    }
+    return 0;
+}
+
 static bool ranges_overlap(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
     if (!a || !b || a_bytes == 0 || b_bytes == 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -790,7 +833,36 @@ GDN_EXPORT gdn_status gdn_step(const gdn_problem* p, const void* q, const void* 
         if (replay->k_out) std::copy(kv.begin(), kv.end(), replay->k_out);
     }
     if (all.empty()) return GDN_OK;
-    return run_jobs(M, all, (cudaStream_t)stream);
+    // On the fused tensor-core path a few long scans (prefills) beside many short ones (resumes, replays) run
+    // best as two launches side by side: the long jobs' CTAs placed first, the short ones on the remaining SMs.
+    // (One launch of all of them places the long CTAs less well; so does letting the short launch reach the
+    // GPU first.)
+    const cudaStream_t cs = (cudaStream_t)stream;
+    const bool fused = use_chunked(p) &&
+                       (p->algo == GDN_ALGO_CHUNKED || (p->algo == GDN_ALGO_AUTO && !two_pass_fits(M, all)));
+    if (fused) {
+        std::stable_sort(all.begin(), all.end(),
+                         [](const HostJob& a, const HostJob& b) { return a.job.len > b.job.len; });
+        SideLane* lane = side_lane();
+        const size_t b = lane ? split_point(all, p->num_heads, lane->sms) : 0;
+        if (b > 0) {
+            std::vector<HostJob> head(all.begin(), all.begin() + b), tail(all.begin() + b, all.end());
+            std::lock_guard<std::mutex> lock(g_side_mutex);   // the lanes' events are shared by every caller
+            if (cudaEventRecord(lane->fork, cs) != cudaSuccess ||
+                cudaStreamWaitEvent(lane->hi, lane->fork, 0) != cudaSuccess ||
+                cudaStreamWaitEvent(lane->lo, lane->fork, 0) != cudaSuccess)
+                return GDN_ERR_CUDA;
+            const gdn_status s1 = run_jobs(M, head, lane->hi);
+            const gdn_status s2 = run_jobs(M, tail, lane->lo);
+            if (cudaEventRecord(lane->join_hi, lane->hi) != cudaSuccess ||
+                cudaEventRecord(lane->join_lo, lane->lo) != cudaSuccess ||
+                cudaStreamWaitEvent(cs, lane->join_hi, 0) != cudaSuccess ||
+                cudaStreamWaitEvent(cs, lane->join_lo, 0) != cudaSuccess)
+                return GDN_ERR_CUDA;
+            return s1 != GDN_OK ? s1 : s2;
+        }
+    }
+    return run_jobs(M, all, cs);
 }
 
 GDN_EXPORT gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, const int64_t* m,

@@ -224,6 +224,16 @@ gdn_status gdn_tail_replay_k(const gdn_problem* p, const void* q, const void* k,
  * replay entry point runs the twin beside the replay in one block, S_exact then
  * agrees with it to rounding rather than bit for bit.
  *
+ * On the tensor-core path, when a few long scans come with many scans at most a
+ * quarter of their length (and the long ones fit on the GPU's multiprocessors at
+ * once), the two groups run as two launches side by side on streams of the
+ * library's own (the long one of the highest priority, so that its blocks are
+ * placed first), forked from `stream` and joined back to it with events: work
+ * enqueued on `stream` before the call is waited for, and work enqueued after it
+ * waits for both launches.  The first such call on a device creates those two
+ * streams and three events (kept until the process exits; make the first call
+ * before any stream capture); calls from several host threads share them.
+ *
  * The parts of one call run at the same time, so none may read what another
  * writes: the resumes read checkpoints stored by earlier calls, and
  * resume->ckpt_states overlapping prefill->ckpt_states is GDN_ERR_INVALID_ARG;
