@@ -1099,13 +1099,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                 *reinterpret_cast<uint32_t*>(smem + OFF_T2H + o) = h2;
                 *reinterpret_cast<uint32_t*>(smem + OFF_T2L + o) = l2;
             };
-            // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 4 (rows 0-31 of G, columns
+            // ---- T = (I + L)^-1 = [[T_AA, 0], [T_BA, T_BB]] in 32-blocks.  Warp 6 (rows 0-31 of G, columns
             //      0-31) and warp 9 (rows 32-63, columns 32-63) each take a whole diagonal 32-block of L and
-            //      invert it alone: two 16x16 forward substitutions and one merge; the gate warp runs a
-            //      chunk ahead.  Then the whole group writes the T operands of both diagonal blocks and merges
+            //      invert it alone: two 16x16 forward substitutions and one merge; the gate warp (7) runs a
+            //      chunk ahead.  Warps 6 and 9 sit on SM sub-partitions 2 and 1 (warp % 4), away from the
+            //      MMA-issue warp's poll loop on sub-partition 0, which slows a warp beside it by ~40 % here.  Then the whole group writes the T operands of both diagonal blocks and merges
             //      the lower-left block.  The merges run on mma.sync with every operand split into bf16
             //      hi + lo. ----
-            if (pw == 0 || pw == 5) {
+            if (pw == 2 || pw == 5) {
                 const int qw = pw == 5 ? 1 : 0;            // diagonal quadrant: rows / columns 32 qw .. + 31
                 {
                     // lanes 0-15: column jc of block 2 qw; lanes 16-31: of block 2 qw + 1 (forward substitution,
