@@ -103,7 +103,7 @@ def lib():
             L.gdn_tail_replay_k.argtypes = [P, vp, vp, vp, vp, vp, pi64, pi64, vp, vp, vp, vp, vp, sz, vp]
             L.gdn_tail_replay_overlap.argtypes = [P, vp, vp, vp, vp, vp, pi64, i32, i32, vp, vp, vp, vp, pi64, pi64,
                                                   vp, vp, sz, vp, sz, vp, vp]
-            L.gdn_adaptive_replay_plan.argtypes = [P, vp, pi64, ctypes.c_float, i32, i32, pi64, pi32]
+            L.gdn_adaptive_replay_plan.argtypes = [P, vp, pi64, ctypes.c_float, i32, i32, pi64, pi32, vp]
             G = ctypes.POINTER(_Group)
             L.gdn_group_scratch_bytes.argtypes = [G, i64]
             L.gdn_group_scratch_bytes.restype = sz
@@ -585,7 +585,7 @@ def gdn_group_replay(h, weights, layers: int, heads: int, d_model: int, d_head: 
 
 
 def gdn_adaptive_replay_plan(alpha, cu_seqlens, m, eps: float, rmax_num: int, rmax_den: int, H: int,
-                             d_k: int = 128, d_v: int = 128):
+                             d_k: int = 128, d_v: int = 128, stream=None):
     """Per-sequence tail length from the gates (see the header): (k list, exact-recovery flags)."""
     cu = _i64(cu_seqlens)
     B = len(cu) - 1
@@ -593,6 +593,7 @@ def gdn_adaptive_replay_plan(alpha, cu_seqlens, m, eps: float, rmax_num: int, rm
     ex = np.zeros(B, dtype=np.int32)
     pr = _problem(cu, H, d_k, d_v, torch.bfloat16, torch.bfloat16)
     rc = lib().gdn_adaptive_replay_plan(ctypes.byref(pr), _ptr(alpha), _p64(_i64(m)), ctypes.c_float(eps),
-                                        rmax_num, rmax_den, _p64(k_out), ex.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+                                        rmax_num, rmax_den, _p64(k_out), ex.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                        _stream(stream, alpha.device))
     _check(rc, "gdn_adaptive_replay_plan")
     return k_out.tolist(), ex.tolist()

@@ -852,8 +852,12 @@ GDN_EXPORT gdn_status gdn_step(const gdn_problem* p, const void* q, const void* 
                 cudaStreamWaitEvent(lane->hi, lane->fork, 0) != cudaSuccess ||
                 cudaStreamWaitEvent(lane->lo, lane->fork, 0) != cudaSuccess)
                 return GDN_ERR_CUDA;
-            const gdn_status s1 = run_jobs(M, head, lane->hi);
-            const gdn_status s2 = run_jobs(M, tail, lane->lo);
+            // Both lanes take the fused kernel: each lane alone might fit the caller's workspace for the two-pass
+            // path, but the two lanes run at the same time and would share its schedule and T areas.
+            LaunchSpec F = M;
+            F.ws_bytes = kWorkspaceBytes;
+            const gdn_status s1 = run_jobs(F, head, lane->hi);
+            const gdn_status s2 = run_jobs(F, tail, lane->lo);
             if (cudaEventRecord(lane->join_hi, lane->hi) != cudaSuccess ||
                 cudaEventRecord(lane->join_lo, lane->lo) != cudaSuccess ||
                 cudaStreamWaitEvent(cs, lane->join_hi, 0) != cudaSuccess ||
@@ -867,7 +871,7 @@ GDN_EXPORT gdn_status gdn_step(const gdn_problem* p, const void* q, const void* 
 
 GDN_EXPORT gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, const int64_t* m,
                                                float eps, int32_t rmax_num, int32_t rmax_den, int64_t* k_out,
-                                               int32_t* exact_out) {
+                                               int32_t* exact_out, gdn_stream_t stream) {
     std::vector<int64_t> lens;
     gdn_status st = check_problem(p, lens);
     if (st != GDN_OK) return st;
@@ -885,8 +889,11 @@ GDN_EXPORT gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float
         if (K > 0) {
             tail.resize((size_t)K * H);
             // gates of rows [m_b - K, m_b): the budget's tail of every head
-            if (cudaMemcpy(tail.data(), alpha + (size_t)(p->cu_seqlens[b] + m[b] - K) * H, sizeof(float) * tail.size(),
-                           cudaMemcpyDeviceToHost) != cudaSuccess)
+            // on the caller's stream, after the work that writes the gates
+            const cudaStream_t cs = (cudaStream_t)stream;
+            if (cudaMemcpyAsync(tail.data(), alpha + (size_t)(p->cu_seqlens[b] + m[b] - K) * H,
+                                sizeof(float) * tail.size(), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+                cudaStreamSynchronize(cs) != cudaSuccess)
                 return GDN_ERR_CUDA;
             for (int h = 0; h < H; ++h) {
                 // smallest k with alpha_m * alpha_{m-1} * ... * alpha_{m-k+1} <= eps (fp32, newest gate first)

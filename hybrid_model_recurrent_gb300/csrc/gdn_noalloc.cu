@@ -39,7 +39,8 @@ GDN_EXPORT gdn_status gdn_prefill_ckpt_noalloc(const gdn_problem* p, const void*
 
     // Per-device set-up: host code may not pass the array's name to a kernel (on the
     // host it is only a stand-in). Ask the runtime for its device address once per
-    // device, with that device current, and reuse it.
+    // device, with that device current, and reuse it for the rest of the process
+    // (a cudaDeviceReset would invalidate it; the header rules that case out).
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return GDN_ERR_CUDA;
     if (dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;

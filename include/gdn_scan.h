@@ -315,13 +315,16 @@ gdn_status gdn_tail_replay_overlap(const gdn_problem* p, const void* q, const vo
  * fp32, newest gate first), and exact_out[b] = 0; when the budget is too short for
  * some head, k_b is the budget and exact_out[b] = 1 (recover that request exactly,
  * e.g. from a checkpoint).
- *  alpha     device [T, H] fp32 (only the budget's tail rows are read; copied to
- *            the host, so the call synchronises with the device)
+ *  alpha     device [T, H] fp32 (only the budget's tail rows are read; they are
+ *            copied to the host on `stream`, which the call then synchronises: work
+ *            enqueued on `stream` before the call, e.g. what writes the gates, is
+ *            complete before they are read)
  *  m         host int64 [B]; eps in [0, 1); rmax_num / rmax_den as in gdn_replay_plan
  *  k_out     host int64 [B]; exact_out host int32 [B]
  */
 gdn_status gdn_adaptive_replay_plan(const gdn_problem* p, const float* alpha, const int64_t* m, float eps,
-                                    int32_t rmax_num, int32_t rmax_den, int64_t* k_out, int32_t* exact_out);
+                                    int32_t rmax_num, int32_t rmax_den, int64_t* k_out, int32_t* exact_out,
+                                    gdn_stream_t stream);
 
 /*
  * In-group chained replay ("Tail-Replay" notes page, section 2.2 step 3 and
@@ -381,8 +384,10 @@ gdn_status gdn_group_replay(const gdn_group* g, const float* h, int64_t m, int32
  * returns GDN_ERR_UNSUPPORTED). Every GPU that loads the library keeps that
  * array until the process exits.
  *  - The first call on each device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it for the rest of the process; make that
+ *    first call before any stream capture.  The cached address does not survive
+ *    cudaDeviceReset (which unloads the library's device code): do not call this
+ *    entry point on a device after resetting it.
  *  - Every call on a device shares the one array. The call clears it on
  *    `stream` before launching, so calls whose work overlaps on the GPU (e.g.
  *    from several host threads on different streams) race on it; serialise them.

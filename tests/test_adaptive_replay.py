@@ -78,14 +78,14 @@ def test_abi_rejects_bad_adaptive_arguments():
     fake = ctypes.c_void_p(0x10000)
     for eps, rn, rd in ((1.0, 1, 10), (-0.1, 1, 10), (float("nan"), 1, 10), (0.1, 2, 1), (0.1, 1, 0)):
         rc = L.gdn_adaptive_replay_plan(ctypes.byref(pr), fake, m.ctypes.data_as(P64), ctypes.c_float(eps), rn, rd,
-                                        k.ctypes.data_as(P64), ex.ctypes.data_as(P32))
+                                        k.ctypes.data_as(P64), ex.ctypes.data_as(P32), None)
         assert rc == gdn.GDN_ERR_INVALID_ARG, (eps, rn, rd)
     m2 = np.array([11], dtype=np.int64)   # m beyond the sequence
     rc = L.gdn_adaptive_replay_plan(ctypes.byref(pr), fake, m2.ctypes.data_as(P64), ctypes.c_float(0.1), 1, 10,
-                                    k.ctypes.data_as(P64), ex.ctypes.data_as(P32))
+                                    k.ctypes.data_as(P64), ex.ctypes.data_as(P32), None)
     assert rc == gdn.GDN_ERR_INVALID_ARG
     rc = L.gdn_adaptive_replay_plan(ctypes.byref(pr), None, m.ctypes.data_as(P64), ctypes.c_float(0.1), 1, 10,
-                                    k.ctypes.data_as(P64), ex.ctypes.data_as(P32))
+                                    k.ctypes.data_as(P64), ex.ctypes.data_as(P32), None)
     assert rc == gdn.GDN_ERR_INVALID_ARG
 
 

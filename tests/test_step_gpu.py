@@ -170,3 +170,39 @@ def test_step_at_full_size_in_the_benchmark_configuration():
             check_output(st["resume"]["o"][lo:hi, h], res["o"], f"step resume o probe {i} h={h}")
         rep = oracle.tail_replay(args[1], args[2], args[3], args[4], m[s], 1, 20)
         assert_close(st["replay"]["S_hat"][s, h], rep["S_hat"], f"step replay s={s} h={h}")
+
+
+def test_step_lanes_never_share_a_two_pass_workspace():
+    """A workspace large enough for the long lane's two-pass path but not for the whole job list: the step
+    runs its two lanes side by side, so neither may take the two-pass path (they would share its schedule and
+    T areas).  Bit for bit the fused kernel's results from the three entry points."""
+    lens = [1024, 1024]
+    H, d = 4, 128
+    w, inp, x = _case(71, lens, H, d, torch.bfloat16)
+    cu = w.cu_seqlens
+    ck = [[256, 512, 768, 1024], [256, 512, 1024]]
+    store = synth.state(73, 7 * H, d, d, 0.7).view(7, H, d, d).to(DEV)
+    probes = [(0, 300), (0, 700), (1, 600), (1, 1000), (0, 256)]
+    m = [1024, 900]
+    L = gdn.lib()
+    head = int(L.gdn_workspace_size_two_pass(sum(lens), H, len(lens)))
+    tail_tokens = sum(d_ - max(c for c in [0] + ck[s] if c <= d_) for s, d_ in probes) + sum(
+        -(-mm // 10) for mm in m)
+    whole = int(L.gdn_workspace_size_two_pass(sum(lens) + tail_tokens, H, len(lens) + len(probes) + len(m)))
+    assert head < whole
+    ws = torch.zeros(head, dtype=torch.uint8, device=DEV)
+    ws_fused = torch.zeros(int(L.gdn_workspace_size()), dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        st = gdn.gdn_step(x.q, x.k, x.v, x.alpha, x.beta, cu, ws=ws, prefill=dict(ckpt_pos=ck),
+                          resume=dict(ckpt_states=store, ckpt_pos=ck, probes=probes),
+                          replay=dict(m=m, r_num=1, r_den=10))
+        pf = gdn.gdn_prefill_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, ckpt_pos=ck, ws=ws_fused, algo="chunked")
+        rs = gdn.gdn_resume_from_ckpt(x.q, x.k, x.v, x.alpha, x.beta, cu, store, ck, probes, ws=ws_fused,
+                                      algo="chunked")
+        rp = gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, m, 1, 10, ws=ws_fused, algo="chunked")
+        torch.cuda.synchronize()
+        assert gdn.read_status(DEV, ws=ws) == gdn.GDN_OK
+        assert torch.equal(st["prefill"]["o"], pf["o"]) and torch.equal(st["prefill"]["S_final"], pf["S_final"])
+        assert torch.equal(st["prefill"]["ckpt_states"], pf["ckpt_states"])
+        assert torch.equal(st["resume"]["S_out"], rs["S_out"]) and torch.equal(st["resume"]["o"], rs["o"])
+        assert torch.equal(st["replay"]["S_hat"], rp["S_hat"])
