@@ -37,9 +37,10 @@
 //   prep (warps 4-11) - the state-independent work of chunk j+1: G, L, T, the
 //       T diag(.) operands, -sigma_0 W, P, and (one warp) the gates and the chunk schedule one
 //       chunk further ahead;
-//   issue (warp 12, one lane) - every tcgen05.mma: the chain's U^T += St (-sigma_0 W)^T, St Q^T,
-//       St += U''^T K, U''^T P^T and the prep's [K; Q] K^T (L and P), W^T, U~^T, each as soon as the
-//       mbarriers of its operands have fired, so that no converting warp waits on a full MMA queue.
+//   issue (warp 12, one lane; without a readout warps 12 and 13, one lane each) - every tcgen05.mma: the
+//       chain's U^T += St (-sigma_0 W)^T, St Q^T, St += U''^T K, U''^T P^T and the prep's [K; Q] K^T (L and
+//       P), W^T, U~^T, each as soon as the mbarriers of its operands have fired, so that no converting warp
+//       waits on a full MMA queue.
 // The prep warps stage the K/Q tiles of chunk j+1 as soon as they have read P_j out of the G
 // columns, so [K; Q] K^T of the next chunk runs beside W^T, U~^T of this one and L is waiting in
 // TMEM when the next iteration starts.
@@ -64,7 +65,8 @@ constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NCHAIN = 128;                  // warps 0-3
 constexpr int NPREP = 256;                   // warps 4-11
-constexpr int NTHREADS = NCHAIN + NPREP + 32;   // + warp 12: MMA issue
+// + warp 12 (MMA issue), and warp 13 (a second MMA-issuing thread) without a readout
+__host__ __device__ constexpr int nthreads(bool readout) { return NCHAIN + NPREP + (readout ? 32 : 64); }
 constexpr int BAR_CHAIN = 1, BAR_PREP = 2;   // named barriers
 constexpr int kRing = 4;                     // chunk schedule entries in flight
 
@@ -382,7 +384,7 @@ __device__ __forceinline__ void drain_phase(uint64_t* b, uint32_t parity, uint64
 // the kernel: one CTA = one (job, head)
 // ------------------------------------------------------------------------------------
 template <bool OUT_BF16, bool READOUT, bool PRE_T>
-__global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(nthreads(READOUT), 1) gdn_chunk_tc_kernel(const __grid_constant__ Params p) {
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
@@ -1280,40 +1282,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
         }
         }
     } else if (lane == 0) {
-        // ============================ MMA issue (warp 12, one lane) ============================
-        // Two streams, each in its own order: prep G_j, WU_j and chain U_j, O1_j, St_j, O2_j; the prep stream
-        // is served first when the prep group bounds the pipeline (T computed here), else the chain.
-        // An item is issued once the mbarriers of its operands have fired; a stream ends after its last chunk.
-        int jc = 0, sc = 0, jp = 0, sp = 0;
-        bool chain_done = false, prep_done = false;
-        uint64_t t_last = global_ns();
-        const uint32_t id64 = idesc(64, false, false), id64b = idesc(64, false, true), id64a = idesc(64, true, false);
-        const uint32_t id128b = idesc(128, false, true);
-        while (!(chain_done && prep_done)) {
-            bool progressed = false;
-            auto serve_prep = [&]() {
-            if (!prep_done) {
-                const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
-                if (sp == 0 && mbar_test(bar_gin, jp & 1)) {
+        // ============================ MMA issue (warp 12, and warp 13 without a readout) ============================
+        if constexpr (!READOUT) {
+            // Without a readout: two issuing threads, one per stream, each in its stream's order: the prep stream
+            // (warp 12) G_j, WU_j and the chain stream (warp 13) U_j, St_j.  An item is issued once the mbarriers of
+            // its operands have fired; each thread blocks in the barrier wait (suspended in hardware, so it takes no
+            // issue slot from the warps that share its SM sub-partition).  Each thread commits its own products; a
+            // product that reads what the other stream wrote waits for that stream's completion barrier.
+            const uint32_t id64 = idesc(64, false, false), id64b = idesc(64, false, true), id64a = idesc(64, true, false);
+            const uint32_t id128b = idesc(128, false, true);
+            auto wait = [&](uint64_t* b, uint32_t parity) { return wait_phase(b, parity, abort_flag, limit); };
+            if (warp == 12) {
+                for (int jp = 0;; ++jp) {
+                    const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
+                    if (!wait(bar_gin, jp & 1)) break;
                     tc_fence_after();
                     // [K; Q] K^T: its K rows give L, its Q rows P (with T given only P, and only with a readout)
                     if (!PRE_T || rd) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                            umma_ss(tbase + TG, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64,
-                                    kk > 0);
+                            umma_ss(tbase + TG, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64, kk > 0);
                         }
                         umma_commit(bar_g);
                         ++cnt[2];
                     }
-                    sp = 1;
-                    progressed = true;
-                }
-                // the U and W columns hold the previous chunk's U'' until its last product (U''^T P^T with a
-                // readout, else the state update) is done
-                if (sp == 1 && mbar_test(bar_wuin, jp & 1) &&
-                    (jp == 0 || mbar_test(rd ? bar_o : bar_st, (jp - 1) & 1))) {
+                    // the U and W columns hold the previous chunk's U'' until its last product (U''^T P^T with a
+                    // readout, else the state update) is done
+                    if (!wait(bar_wuin, jp & 1)) break;
+                    if (jp > 0 && !wait(rd ? bar_o : bar_st, (jp - 1) & 1)) break;
                     tc_fence_after();
                     // W^T = K^T T1^T, U~^T = V^T T2^T
                     const uint32_t inV = sbase + OFF_V;
@@ -1328,39 +1325,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                     }
                     umma_commit(bar_wu);
                     ++cnt[3];
-                    progressed = true;
-                    if (ring[jp % kRing].last) prep_done = true;
-                    else {
-                        ++jp;
-                        sp = 0;
-                    }
+                    if (ring[jp % kRing].last) break;
                 }
-            }
-            };
-            auto serve_chain = [&]() {
-            if (!chain_done) {
-                const Ring& R = ring[jc % kRing];
-                const uint32_t inKQ = sbase + OFF_KQ + (jc & 1) * 32768;
-                if (sc == 0) {
-                    if (mbar_test(bar_split, jc & 1) && mbar_test(bar_wready, jc & 1)) {
-                        tc_fence_after();
-                        // U^T += St (-sigma_0 W)^T  (St from TMEM as bf16 hi/lo pairs)
+            } else if (warp == 13) {
+                for (int jc = 0;; ++jc) {
+                    const Ring& R = ring[jc % kRing];
+                    const uint32_t inKQ = sbase + OFF_KQ + (jc & 1) * 32768;
+                    if (!wait(bar_split, jc & 1) || !wait(bar_wready, jc & 1)) break;
+                    tc_fence_after();
+                    // U^T += St (-sigma_0 W)^T  (St from TMEM as bf16 hi/lo pairs)
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bwh = sdesc(sbase + OFF_WH + kk * 2048, 16384, 1024);
-                            const uint32_t ah = tbase + T_SH + 8 * kk, al = tbase + T_SL + 8 * kk;
-                            // [U | W] += S_hi [W_hi | W_lo]^T (N = 128: W_lo follows W_hi at the block stride)
-                            umma_ts(tbase + T_U, ah, bwh, id128b, 1);
-                            umma_ts(tbase + T_U, al, bwh, id64b, 1);
-                        }
-                        umma_commit(bar_uo);
-                        ++cnt[4];
-                        sc = rd ? 1 : 2;
-                        progressed = true;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bwh = sdesc(sbase + OFF_WH + kk * 2048, 16384, 1024);
+                        const uint32_t ah = tbase + T_SH + 8 * kk, al = tbase + T_SL + 8 * kk;
+                        // [U | W] += S_hi [W_hi | W_lo]^T (N = 128: W_lo follows W_hi at the block stride)
+                        umma_ts(tbase + T_U, ah, bwh, id128b, 1);
+                        umma_ts(tbase + T_U, al, bwh, id64b, 1);
                     }
-                }
-                if (sc == 1) {
-                    if (jc == 0 || mbar_test(bar_ofree, (jc - 1) & 1)) {
+                    umma_commit(bar_uo);
+                    ++cnt[4];
+                    if (rd) {
+                        if (jc > 0 && !wait(bar_ofree, (jc - 1) & 1)) break;
                         tc_fence_after();
                         // O^T = St Q^T
 #pragma unroll
@@ -1369,28 +1354,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                             umma_ts(tbase + TO, tbase + T_SH + 8 * kk, bq, id64, kk > 0);
                             umma_ts(tbase + TO, tbase + T_SL + 8 * kk, bq, id64, 1);
                         }
-                        sc = 2;
-                        progressed = true;
                     }
-                }
-                if (sc == 2) {
-                    if (mbar_test(bar_ufree, jc & 1)) {
-                        tc_fence_after();
-                        // St += U''^T K
+                    if (!wait(bar_ufree, jc & 1)) break;
+                    tc_fence_after();
+                    // St += U''^T K
 #pragma unroll
-                        for (int kt = 0; kt < 4; ++kt) {
-                            const uint64_t bk = sdesc(inKQ + kt * 2048, 16384, 1024);   // K: MN-major over d_k
-                            umma_ts(tbase + T_S, tbase + T_U + 8 * kt, bk, id128b, 1);   // U'' hi
-                            umma_ts(tbase + T_S, tbase + TW + 8 * kt, bk, id128b, 1);    // U'' lo
-                        }
-                        umma_commit(bar_st);
-                        ++cnt[5];
-                        sc = rd ? 3 : 4;
-                        progressed = true;
+                    for (int kt = 0; kt < 4; ++kt) {
+                        const uint64_t bk = sdesc(inKQ + kt * 2048, 16384, 1024);   // K: MN-major over d_k
+                        umma_ts(tbase + T_S, tbase + T_U + 8 * kt, bk, id128b, 1);   // U'' hi
+                        umma_ts(tbase + T_S, tbase + TW + 8 * kt, bk, id128b, 1);    // U'' lo
                     }
-                }
-                if (sc == 3) {
-                    if (mbar_test(bar_pready, jc & 1)) {
+                    umma_commit(bar_st);
+                    ++cnt[5];
+                    if (rd) {
+                        if (!wait(bar_pready, jc & 1)) break;
                         tc_fence_after();
                         if (!R.single) {
                             // O^T += U''^T P^T
@@ -1405,35 +1382,168 @@ __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_tc_kernel(const __grid_
                         }
                         umma_commit(bar_o);
                         ++cnt[6];
-                        sc = 4;
+                    }
+                    if (R.last) break;
+                }
+            }
+        } else if (warp == 12) {
+            // With a readout: one thread polls both streams and serves the prep's products first.  (Measured: two
+            // sleeping threads shorten the replays, whose chain is short, and lengthen the prefill, where the
+            // order in which the single thread interleaves the streams matters more.)
+            // Two streams, each in its own order: prep G_j, WU_j and chain U_j, O1_j, St_j, O2_j; the prep stream
+            // is served first when the prep group bounds the pipeline (T computed here), else the chain.
+            // An item is issued once the mbarriers of its operands have fired; a stream ends after its last chunk.
+            int jc = 0, sc = 0, jp = 0, sp = 0;
+            bool chain_done = false, prep_done = false;
+            uint64_t t_last = global_ns();
+            const uint32_t id64 = idesc(64, false, false), id64b = idesc(64, false, true), id64a = idesc(64, true, false);
+            const uint32_t id128b = idesc(128, false, true);
+            while (!(chain_done && prep_done)) {
+                bool progressed = false;
+                auto serve_prep = [&]() {
+                if (!prep_done) {
+                    const uint32_t inKQ = sbase + OFF_KQ + (jp & 1) * 32768;
+                    if (sp == 0 && mbar_test(bar_gin, jp & 1)) {
+                        tc_fence_after();
+                        // [K; Q] K^T: its K rows give L, its Q rows P (with T given only P, and only with a readout)
+                        if (!PRE_T || rd) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                                umma_ss(tbase + TG, sdesc(inKQ + off, 16, 1024), sdesc(inKQ + off, 16, 1024), id64,
+                                        kk > 0);
+                            }
+                            umma_commit(bar_g);
+                            ++cnt[2];
+                        }
+                        sp = 1;
                         progressed = true;
                     }
-                }
-                if (sc == 4) {
-                    if (R.last) chain_done = true;
-                    else {
-                        ++jc;
-                        sc = 0;
+                    // the U and W columns hold the previous chunk's U'' until its last product (U''^T P^T with a
+                    // readout, else the state update) is done
+                    if (sp == 1 && mbar_test(bar_wuin, jp & 1) &&
+                        (jp == 0 || mbar_test(rd ? bar_o : bar_st, (jp - 1) & 1))) {
+                        tc_fence_after();
+                        // W^T = K^T T1^T, U~^T = V^T T2^T
+                        const uint32_t inV = sbase + OFF_V;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ak = sdesc(inKQ + ks * 2048, 16384, 1024);   // K^T: MN-major, d_k blocks 16 KB apart
+                            const uint64_t av = sdesc(inV + ks * 2048, 8192, 1024);     // V^T: MN-major, d_v blocks 8 KB apart
+                            umma_ss(tbase + TW, ak, sdesc(sbase + OFF_T1H + ks * 32, 16, 1024), id64a, ks > 0);
+                            umma_ss(tbase + TW, ak, sdesc(sbase + OFF_T1L + ks * 32, 16, 1024), id64a, 1);
+                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2H + ks * 32, 16, 1024), id64a, ks > 0);
+                            umma_ss(tbase + T_U, av, sdesc(sbase + OFF_T2L + ks * 32, 16, 1024), id64a, 1);
+                        }
+                        umma_commit(bar_wu);
+                        ++cnt[3];
+                        progressed = true;
+                        if (ring[jp % kRing].last) prep_done = true;
+                        else {
+                            ++jp;
+                            sp = 0;
+                        }
                     }
                 }
-            }
-            };
-            // with T computed beforehand the state chain is the critical path: its products go first
-            if (PRE_T) {
-                serve_chain();
-                serve_prep();
-            } else {
-                serve_prep();
-                serve_chain();
-            }
-            if (progressed) {
-                t_last = global_ns();
-            } else {
-                __nanosleep(20);
-                if (*abort_flag) break;
-                if (global_ns() - t_last > limit) {
-                    *abort_flag = 1;
-                    break;
+                };
+                auto serve_chain = [&]() {
+                if (!chain_done) {
+                    const Ring& R = ring[jc % kRing];
+                    const uint32_t inKQ = sbase + OFF_KQ + (jc & 1) * 32768;
+                    if (sc == 0) {
+                        if (mbar_test(bar_split, jc & 1) && mbar_test(bar_wready, jc & 1)) {
+                            tc_fence_after();
+                            // U^T += St (-sigma_0 W)^T  (St from TMEM as bf16 hi/lo pairs)
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bwh = sdesc(sbase + OFF_WH + kk * 2048, 16384, 1024);
+                                const uint32_t ah = tbase + T_SH + 8 * kk, al = tbase + T_SL + 8 * kk;
+                                // [U | W] += S_hi [W_hi | W_lo]^T (N = 128: W_lo follows W_hi at the block stride)
+                                umma_ts(tbase + T_U, ah, bwh, id128b, 1);
+                                umma_ts(tbase + T_U, al, bwh, id64b, 1);
+                            }
+                            umma_commit(bar_uo);
+                            ++cnt[4];
+                            sc = rd ? 1 : 2;
+                            progressed = true;
+                        }
+                    }
+                    if (sc == 1) {
+                        if (jc == 0 || mbar_test(bar_ofree, (jc - 1) & 1)) {
+                            tc_fence_after();
+                            // O^T = St Q^T
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bq = sdesc(inKQ + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                                umma_ts(tbase + TO, tbase + T_SH + 8 * kk, bq, id64, kk > 0);
+                                umma_ts(tbase + TO, tbase + T_SL + 8 * kk, bq, id64, 1);
+                            }
+                            sc = 2;
+                            progressed = true;
+                        }
+                    }
+                    if (sc == 2) {
+                        if (mbar_test(bar_ufree, jc & 1)) {
+                            tc_fence_after();
+                            // St += U''^T K
+#pragma unroll
+                            for (int kt = 0; kt < 4; ++kt) {
+                                const uint64_t bk = sdesc(inKQ + kt * 2048, 16384, 1024);   // K: MN-major over d_k
+                                umma_ts(tbase + T_S, tbase + T_U + 8 * kt, bk, id128b, 1);   // U'' hi
+                                umma_ts(tbase + T_S, tbase + TW + 8 * kt, bk, id128b, 1);    // U'' lo
+                            }
+                            umma_commit(bar_st);
+                            ++cnt[5];
+                            sc = rd ? 3 : 4;
+                            progressed = true;
+                        }
+                    }
+                    if (sc == 3) {
+                        if (mbar_test(bar_pready, jc & 1)) {
+                            tc_fence_after();
+                            if (!R.single) {
+                                // O^T += U''^T P^T
+#pragma unroll
+                                for (int kt = 0; kt < 4; ++kt) {
+                                    const uint64_t bph = sdesc(sbase + OFF_PH + kt * 32, 16, 1024);
+                                    const uint64_t bpl = sdesc(sbase + OFF_PL + kt * 32, 16, 1024);
+                                    umma_ts(tbase + TO, tbase + T_U + 8 * kt, bph, id64, 1);
+                                    umma_ts(tbase + TO, tbase + T_U + 8 * kt, bpl, id64, 1);
+                                    umma_ts(tbase + TO, tbase + TW + 8 * kt, bph, id64, 1);
+                                }
+                            }
+                            umma_commit(bar_o);
+                            ++cnt[6];
+                            sc = 4;
+                            progressed = true;
+                        }
+                    }
+                    if (sc == 4) {
+                        if (R.last) chain_done = true;
+                        else {
+                            ++jc;
+                            sc = 0;
+                        }
+                    }
+                }
+                };
+                // with T computed beforehand the state chain is the critical path: its products go first
+                if (PRE_T) {
+                    serve_chain();
+                    serve_prep();
+                } else {
+                    serve_prep();
+                    serve_chain();
+                }
+                if (progressed) {
+                    t_last = global_ns();
+                } else {
+                    __nanosleep(20);
+                    if (*abort_flag) break;
+                    if (global_ns() - t_last > limit) {
+                        *abort_flag = 1;
+                        break;
+                    }
                 }
             }
         }
@@ -1465,7 +1575,7 @@ cudaError_t launch_chunk_tc(const Params& p, int grid, cudaStream_t stream) {
     static std::atomic<int> optin[kMaxOptinDevices];
     cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), kSmemBytes, optin);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NTHREADS, kSmemBytes, stream>>>(p);
+    kern<<<grid, nthreads(READOUT), kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
