@@ -769,11 +769,11 @@ def run_ours(args, ws, rank, local):
             "phases": {k: v for k, v in step.tok_head.items()},
             "states_per_s": sum(len(c) for c in step.ck) * w.H * args.steps / slowest,
             "cpu_baseline": base,
-            "placement": placement_report(),
-            "replay_overlap": overlap_report(dev),
-            "chunked_variants": two_pass_report(step),
+            "placement": None if args.step_only else placement_report(),
+            "replay_overlap": None if args.step_only else overlap_report(dev),
+            "chunked_variants": None if args.step_only else two_pass_report(step),
             "step_forms": step_forms_report(step),
-            "workloads": workloads_report(dev, hbm_peak),
+            "workloads": None if args.step_only else workloads_report(dev, hbm_peak),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -786,6 +786,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the step (and its three-call form) only: no placement, overlap, chunked-variant or "
+                         "other-workload reports (a few GB on the device, for profiler captures)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     if args.impl == "reference":
