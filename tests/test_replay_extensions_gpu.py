@@ -90,6 +90,32 @@ def test_adaptive_plan_matches_oracle_and_meets_the_bound():
             assert float(torch.linalg.norm(E[s, h])) <= bound * (1 + 1e-3) + 1e-5, (s, h)
 
 
+def test_adaptive_plan_reads_the_gates_after_earlier_work_on_its_stream():
+    """The plan copies the gates on the caller's stream: gates that earlier work on that stream is still writing (here
+    a copy queued behind a device-side delay, on a non-blocking stream) are the ones it reads."""
+    lens = [800, 600]
+    H = 2
+    w, inp = _inputs(87, lens, H, 128, torch.bfloat16, 0.9, 1.0)
+    cu = w.cu_seqlens
+    m = [800, 600]
+    eps, rmax = 1e-2, (1, 2)
+    fast = inp.alpha * 0.5                 # forgets within a few tokens
+    slow = torch.ones_like(inp.alpha)      # never forgets: the budget is too short for every head
+    want_fast = oracle.adaptive_replay_plan(fast, cu, m, eps, *rmax)
+    want_slow = oracle.adaptive_replay_plan(slow, cu, m, eps, *rmax)
+    assert want_fast != want_slow
+    side = torch.cuda.Stream()
+    alpha_d = slow.to(DEV)
+    fast_h = fast.pin_memory()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(20_000_000)          # ~10 ms on the side stream before the gates change
+        alpha_d.copy_(fast_h, non_blocking=True)
+    got = gdn.gdn_adaptive_replay_plan(alpha_d, cu, m, eps, *rmax, H=H, stream=side)
+    assert got == want_fast, "the plan must see the gates written before it on its stream"
+    torch.cuda.synchronize()
+
+
 def _timed(stream, fn, reps=5):
     fn()
     torch.cuda.synchronize()
