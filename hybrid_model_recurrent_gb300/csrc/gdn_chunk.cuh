@@ -111,8 +111,9 @@ template <bool OUT_BF16, bool READOUT>
 __global__ void __launch_bounds__(NTHREADS, 1) gdn_chunk_kernel(const __grid_constant__ Params p) {
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
+    // aligned by pointer arithmetic on the shared array (not through an integer), so that the compiler keeps
+    // its address space and plain C++ accesses below compile to shared-memory loads and stores
+    unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     float* sc_g = reinterpret_cast<float*>(smem + OFF_SC);

@@ -45,8 +45,14 @@ constexpr int kChunk = 32;     // tokens per pipeline stage
 constexpr int kStages = 3;     // depth of the shared-memory ring
 constexpr int kMaxJobs = 256;  // jobs per launch (host splits larger batches)
 constexpr int kMaxCkpts = 1536;
+// A lane holds kRowSlots state rows x (d_k / kColLanes) columns; the rows split into two groups that run half
+// a token apart (see the consumer loop).  Shared memory delivers 32 floats a cycle to an SM and every float of
+// k or q a lane loads feeds one FMA per row it holds, so 4 rows keep the loads under the FMA time, and the 64
+// registers of a d_k = 128 tile leave room for 8 consumer warps (two per SM sub-partition) at 168 registers.
+constexpr int kColLanes = 8;
+constexpr int kRowSlots = 4;
 constexpr int kMaxConsumerWarps = 8;
-constexpr int kSlotsPerWarp = 16;   // state rows (slots) held by one consumer warp
+constexpr int kSlotsPerWarp = (32 / kColLanes) * kRowSlots;   // state rows (slots) held by one consumer warp
 constexpr float kRenormFloor = 0x1p-32f;
 // Bound of the wait for this CTA's own copies in flight before it exits (independent of the
 // user's wait limit, so that even a tiny limit never lets a CTA leave with a copy pending).
@@ -140,6 +146,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// the same probe, letting the hardware suspend the thread for up to `hint_ns` while the phase is pending
+// (it resumes as soon as the phase completes), so that a long wait issues a few instructions, not a spin
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, "
+        "p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -150,8 +168,11 @@ __device__ __forceinline__ uint64_t global_ns() {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
+        // suspend in slices of at most 1/8 of the limit (and 20 us), so that the limit is still honoured
+        const uint64_t slice = limit_ns / 8;
+        const uint32_t hint = slice < 20000u ? (uint32_t)slice : 20000u;
         const uint64_t t0 = global_ns();
-        while (!(ok = mbar_try_wait(bar, parity))) {
+        while (!(ok = mbar_try_wait_suspend(bar, parity, hint))) {
             if (global_ns() - t0 > limit_ns) break;
         }
     }
@@ -179,26 +200,27 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Reduce over the 8 column lanes of a row group.  On entry v[i] is this lane's
-// partial sum for slot i (4 slots); on exit the return value is the full sum of
-// slot (cl >> 1) & 3, held by lanes cl = 2s and 2s+1 of the group.
-__device__ __forceinline__ float reduce_slots(float (&v)[4], int lane) {
-    {
-        const bool up = (lane & 4) != 0;
+// Reduce over the NCL column lanes of a row group.  On entry v[i] is this lane's partial sum for slot i
+// (RT slots); on exit the return value is the full sum of slot cl / (NCL / RT), held by the NCL / RT lanes
+// of the group with that quotient.  Each round of the reduce-scatter halves the slots a lane carries (the
+// lanes with the round's bit set keep the upper half); the lanes left sharing a slot then add up.
+template <int NCL, int RT>
+__device__ __forceinline__ float reduce_slots(float (&v)[RT], int lane) {
+    static_assert(NCL >= RT && (NCL & (NCL - 1)) == 0 && (RT & (RT - 1)) == 0, "lane split");
+    int step = NCL / 2;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float send = up ? v[i] : v[i + 2];
-            const float keep = up ? v[i + 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    for (int n = RT; n > 1; n /= 2, step /= 2) {
+        const bool up = (lane & step) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
         }
     }
-    {
-        const bool up = (lane & 2) != 0;
-        const float send = up ? v[0] : v[1];
-        const float keep = up ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+#pragma unroll
+    for (; step >= 1; step /= 2) v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], step);
+    return v[0];
 }
 
 // Shared-memory layout of one pipeline stage.
@@ -245,8 +267,10 @@ template <int DK, bool IN_BF16, bool OUT_BF16, bool READOUT, bool TWIN>
 __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     gdn_scan_kernel(const __grid_constant__ Params p) {
     constexpr int ES = IN_BF16 ? 2 : 4;
-    constexpr int NCL = 8;                   // column lanes per row group
-    constexpr int RT = 4;                    // row slots per lane
+    constexpr int NCL = kColLanes;           // column lanes per row group
+    constexpr int RT = kRowSlots;            // row slots per lane
+    constexpr int RG = RT / 2;               // slots of one of the lane's two row groups (A: 0..RG-1, B: RG..)
+    constexpr int LPG = NCL / RG;            // lanes that end up holding one slot's sums in a group reduction
     constexpr int CT = DK / NCL;             // columns per lane (16, 8, 4)
     constexpr int CT2 = CT / 2;
     constexpr int CH4 = CT / 4;              // fp32 float4 chunks per lane and vector
@@ -257,9 +281,10 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     static_assert(NRG * RT == kSlotsPerWarp, "slots per warp");
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
 
+    // the 128-byte aligned base is formed by pointer arithmetic on the shared array (not through an integer),
+    // so that the compiler keeps its address space and reads the stages with shared-memory loads
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127u) & ~uintptr_t(127));
+    unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
 
     const int nw = p.nw;
     const int RB = p.rows_per_cta;
@@ -392,12 +417,16 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     }
 
     // ================================ consumer warps ===============================
+    // The lane's RT slots form two row groups, A (slots 0..RG-1) and B (RG..RT-1), run half a token apart:
+    // group B's reduction, c and readout of one token are issued between group A's FMAs of the next, and
+    // group A's between group B's, so that neither group waits for its own shuffles.  With the twin, A is
+    // the scan and B the twin.
     const int cl = lane & (NCL - 1);
     const int rg = lane / NCL;
-    const int my_slot = (cl >> 1) & 3;                                   // slot whose sums this lane holds
-    const int my_state = TWIN ? (my_slot / HALF) : 0;
     const int row0 = warp * WR + rg * HALF;                              // CTA row of this group's slot 0
-    const int my_row = row0 + (TWIN ? (my_slot % HALF) : my_slot);       // CTA-relative real row
+    const int gslot = cl / LPG;                                          // slot (within a group) of this lane's sums
+    const int rowA = row0 + gslot;                                       // CTA-relative real rows of those slots
+    const int rowB = row0 + (TWIN ? gslot : RG + gslot);
     const int grow_base = rb * RB + row0;                                // head row of slot 0
     const size_t head_state = (size_t)h * (size_t)dv * DK;
 
@@ -417,37 +446,84 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
     }
 
-    auto load_vec = [&](const unsigned char* tok, float2 (&dst)[CT2]) {
-        const float4* p4 = reinterpret_cast<const float4*>(tok);
-#pragma unroll
-        for (int j4 = 0; j4 < CH4; ++j4) {
-            const float4 w = p4[cl + NCL * j4];
-            dst[2 * j4 + 0] = make_float2(w.x, w.y);
-            dst[2 * j4 + 1] = make_float2(w.z, w.w);
-        }
+    // this lane's 4-column piece j4 of a staged fp32 vector (k or q of one token)
+    auto piece = [&](const unsigned char* tok, int j4, float2& lo, float2& hi) {
+        const float4 w = reinterpret_cast<const float4*>(tok)[cl + NCL * j4];
+        lo = make_float2(w.x, w.y);
+        hi = make_float2(w.z, w.w);
     };
-    auto load_v = [&](const unsigned char* stage, int tau) -> float {
-        const unsigned char* pv = stage + L.v_off + ((size_t)tau * RB + my_row) * ES;
+    auto load_v = [&](const unsigned char* stage, int tau, int row) -> float {
+        const unsigned char* pv = stage + L.v_off + ((size_t)tau * RB + row) * ES;
         if constexpr (IN_BF16)
             return __uint_as_float(((uint32_t) * reinterpret_cast<const unsigned short*>(pv)) << 16);
         else
             return *reinterpret_cast<const float*>(pv);
     };
-    auto dot_slots = [&](const float2 (&x)[CT2], float (&out)[RT]) {
-        float2 acc[RT];
+    // per-slot partial sums of St x over this lane's columns for the slots g*RG .. g*RG+RG-1
+    auto dot_group = [&](int g, const unsigned char* x, float (&out)[RG]) {
+        float2 acc[RG];
 #pragma unroll
-        for (int i = 0; i < RT; ++i) acc[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < RG; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int jj = 0; jj < CT2; ++jj)
+        for (int j4 = 0; j4 < CH4; ++j4) {
+            float2 x0, x1;
+            piece(x, j4, x0, x1);
 #pragma unroll
-            for (int i = 0; i < RT; ++i) acc[i] = __ffma2_rn(S[i][jj], x[jj], acc[i]);
+            for (int i = 0; i < RG; ++i) acc[i] = __ffma2_rn(S[g * RG + i][2 * j4], x0, acc[i]);
 #pragma unroll
-        for (int i = 0; i < RT; ++i) out[i] = acc[i].x + acc[i].y;
+            for (int i = 0; i < RG; ++i) acc[i] = __ffma2_rn(S[g * RG + i][2 * j4 + 1], x1, acc[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < RG; ++i) out[i] = acc[i].x + acc[i].y;
     };
-    auto broadcast_c = [&](float c_mine, float (&creg)[RT]) {
+    // c = (beta / s) v - beta (St k) from the token's scalars {s, beta / s, beta, flags}, rounded the same way
+    // at every call site (an explicit FMA, never a contraction the compiler chooses per site), so that the
+    // restart after a checkpoint and a resumed job's first token agree bit for bit
+    auto c_of = [](const float4& sc, float v, float pk) { return __fmaf_rn(sc.y, v, -__fmul_rn(sc.z, pk)); };
+    // c of the group's slot whose sums this lane holds, to every column lane of its row group (as (c, c))
+    auto broadcast_c = [&](float c_mine, float2 (&cc)[RG]) {
         const int grp = lane & ~(NCL - 1);
 #pragma unroll
-        for (int i = 0; i < RT; ++i) creg[i] = __shfl_sync(0xffffffffu, c_mine, grp | (i << 1));
+        for (int i = 0; i < RG; ++i) {
+            const float c = __shfl_sync(0xffffffffu, c_mine, grp | (i * LPG));
+            cc[i] = make_float2(c, c);
+        }
+    };
+    // one group's pass over token t: St += c k_t^T, then the partial sums of St k_{t+1} and St q_t
+    auto group_pass = [&](int g, const float2 (&cc)[RG], const float2 (&kc)[CT2], const float2 (&kn)[CT2],
+                          const unsigned char* qtok, float (&pk)[RG], float (&pq)[RG]) {
+        float2 ak[RG], aq[RG];
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+            ak[i] = make_float2(0.f, 0.f);
+            aq[i] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int j4 = 0; j4 < CH4; ++j4) {
+            float2 q0 = make_float2(0.f, 0.f), q1 = make_float2(0.f, 0.f);
+            if constexpr (READOUT) piece(qtok, j4, q0, q1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int jj = 2 * j4 + e;
+                const float2 qe = e ? q1 : q0;
+#pragma unroll
+                for (int i = 0; i < RG; ++i) {
+                    float2& x = S[g * RG + i][jj];
+                    x = __ffma2_rn(cc[i], kc[jj], x);
+                    ak[i] = __ffma2_rn(x, kn[jj], ak[i]);
+                    if constexpr (READOUT) aq[i] = __ffma2_rn(x, qe, aq[i]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+            pk[i] = ak[i].x + ak[i].y;
+            pq[i] = aq[i].x + aq[i].y;
+        }
+    };
+    auto load_k = [&](const unsigned char* tok, float2 (&k)[CT2]) {
+#pragma unroll
+        for (int j4 = 0; j4 < CH4; ++j4) piece(tok, j4, k[2 * j4], k[2 * j4 + 1]);
     };
     // write the slots of one state (0: the scan, 1: the twin) to dst_head [dv, dk]
     auto store_state = [&](float* dst_head, int which) {
@@ -464,122 +540,126 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
     };
 
-    bool ok = true;
-    float creg[RT];
-    float2 kc[CT2];
-    float4 sct = make_float4(1.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < RT; ++i) creg[i] = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < CT2; ++jj) kc[jj] = make_float2(0.f, 0.f);
+    void* const o_job = p.jobs[job_idx].o;
+    OutT* const o_head = reinterpret_cast<OutT*>(o_job) + (size_t)h * (size_t)dv + (size_t)(rb * RB);
+    const bool o_lane = READOUT && o_job != nullptr && (cl % LPG) == 0;
+    auto store_o = [&](OutT* o_tok, int row, float val) {
+        OutT* op = o_tok + row;
+        if constexpr (OUT_BF16)
+            *op = __float2bfloat16_rn(val);
+        else
+            *op = val;
+    };
 
+    // Restart from the state in registers before token t of stage `stg` at row tau (the job start, and after
+    // every renormalisation): group A's c_t from a direct St k_t, group B's partial sums of St k_t.
+    float2 ccA[RG], ccB[RG];
+    float pBk[RG], pBq[RG];
+    auto restart = [&](const unsigned char* ktok, const float4& sc, const unsigned char* stg, int tau) {
+        float pk[RG];
+        dot_group(0, ktok, pk);
+        const float pkr = reduce_slots<NCL, RG>(pk, lane);
+        broadcast_c(c_of(sc, load_v(stg, tau, rowA), pkr), ccA);
+        dot_group(1, ktok, pBk);
+    };
+
+    bool ok = true;
+    float4 sct = make_float4(1.f, 0.f, 0.f, 0.f);   // scalars of the current token
+    float4 scp = sct;                               // scalars of the token before
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+        ccA[i] = ccB[i] = make_float2(0.f, 0.f);
+        pBk[i] = pBq[i] = 0.f;
+    }
     if (len > 0) {
         ok = warp_wait(&full[0], 0u, limit);
         if (ok) {
-            load_vec(smem + L.kf_off, kc);
-            float pk[RT];
-            dot_slots(kc, pk);
-            const float pkr = reduce_slots(pk, lane);
             sct = reinterpret_cast<const float4*>(smem + L.sc_off)[0];
-            const float vv = load_v(smem, 0);
-            broadcast_c(sct.y * vv - sct.z * pkr, creg);
+            restart(smem + L.kf_off, sct, smem, 0);
         }
     }
 
-    void* const o_job = p.jobs[job_idx].o;
-    OutT* const o_base = reinterpret_cast<OutT*>(o_job) + (size_t)h * (size_t)dv + (size_t)(rb * RB + my_row);
-    const bool o_lane = READOUT && o_job != nullptr && my_state == 0 && (cl & 1) == 0;
-    for (int tg = 0; ok && tg < len; ++tg) {
-        const int c = tg / kChunk;
-        const int tau = tg - c * kChunk;
+    // Chunks of the stage ring outside, tokens inside: per token only pointer steps, no index division.
+    OutT* o_t = o_head;   // output row of the current token
+    const size_t o_step = (size_t)H * (size_t)dv;
+    int tg = 0;
+    for (int c = 0; ok && c < nchunks; ++c) {
         const int st = c % kStages;
-        const bool has_next = tg + 1 < len;
-        const int cn = (tg + 1) / kChunk;
-        const int taun = tg + 1 - cn * kChunk;
-        const int stn = cn % kStages;
-        unsigned char* stage = smem + (size_t)st * L.bytes;
-        unsigned char* stage_n = smem + (size_t)stn * L.bytes;
-        if (has_next && taun == 0) {
-            if (!warp_wait(&full[stn], (uint32_t)((cn / kStages) & 1), limit)) {
-                ok = false;
-                break;
-            }
-        }
-        float2 kn[CT2];
-        if (has_next) {
-            load_vec(stage_n + L.kf_off + (size_t)taun * DK * 4, kn);
-        } else {
-#pragma unroll
-            for (int jj = 0; jj < CT2; ++jj) kn[jj] = make_float2(0.f, 0.f);
-        }
-        // pass A: St += c k_t^T, then the next token's St k_{t+1}
-        float pk[RT];
-        {
-            float2 acc[RT];
-            float2 cc[RT];
-#pragma unroll
-            for (int i = 0; i < RT; ++i) {
-                acc[i] = make_float2(0.f, 0.f);
-                cc[i] = make_float2(creg[i], creg[i]);
-            }
-#pragma unroll
-            for (int jj = 0; jj < CT2; ++jj)
-#pragma unroll
-                for (int i = 0; i < RT; ++i) {
-                    S[i][jj] = __ffma2_rn(cc[i], kc[jj], S[i][jj]);
-                    acc[i] = __ffma2_rn(S[i][jj], kn[jj], acc[i]);
+        const int stn = (c + 1) % kStages;
+        const unsigned char* stage = smem + (size_t)st * L.bytes;
+        const unsigned char* stage_n = smem + (size_t)stn * L.bytes;
+        const int n = min(kChunk, len - c * kChunk);
+        const bool more = c + 1 < nchunks;
+        for (int tau = 0; tau < n; ++tau, ++tg, o_t += o_step) {
+            const bool edge = tau == n - 1;   // the next token, if any, is the next stage's first
+            if (edge && more) {
+                if (!warp_wait(&full[stn], (uint32_t)(((c + 1) / kStages) & 1), limit)) {
+                    ok = false;
+                    break;
                 }
-#pragma unroll
-            for (int i = 0; i < RT; ++i) pk[i] = acc[i].x + acc[i].y;
-        }
-        float pkr = reduce_slots(pk, lane);
-        float4 scn = make_float4(1.f, 0.f, 0.f, 0.f);
-        float vv = 0.f;
-        if (has_next) {
-            scn = reinterpret_cast<const float4*>(stage_n + L.sc_off)[taun];
-            vv = load_v(stage_n, taun);
-        }
-        if constexpr (READOUT) {
-            // pass B: readout St q_t of the post-update state
-            float2 qv[CT2];
-            load_vec(stage + L.qf_off + (size_t)tau * DK * 4, qv);
-            float pq[RT];
-            dot_slots(qv, pq);
-            const float pqr = reduce_slots(pq, lane);
-            if (o_lane) {
-                const float ov = sct.x * pqr;
-                OutT* op = o_base + (size_t)tg * (size_t)H * (size_t)dv;
-                if constexpr (OUT_BF16)
-                    *op = __float2bfloat16_rn(ov);
-                else
-                    *op = ov;
             }
-        }
-        const uint32_t fl = __float_as_uint(sct.w);
-        if (fl & FLAG_RENORM) {
-            const float2 ss = make_float2(sct.x, sct.x);
-#pragma unroll
-            for (int i = 0; i < RT; ++i)
-#pragma unroll
-                for (int jj = 0; jj < CT2; ++jj) S[i][jj] = __fmul2_rn(S[i][jj], ss);
-            if (has_next) {
-                dot_slots(kn, pk);
-                pkr = reduce_slots(pk, lane);
+            const bool has_next = !edge || more;
+            const unsigned char* nst = edge ? stage_n : stage;
+            const int taun = edge ? 0 : tau + 1;
+            // k of the next token (the last token dots with its own k; those sums are never used).  Past the last
+            // token the next-token reads below stay inside the stage ring and are not used either.
+            const unsigned char* k_cur = stage + L.kf_off + (size_t)tau * DK * 4;
+            const unsigned char* k_nxt = has_next ? nst + L.kf_off + (size_t)taun * DK * 4 : k_cur;
+            const unsigned char* q_cur = stage + L.qf_off + (size_t)tau * DK * 4;
+            const float4 scn = reinterpret_cast<const float4*>(nst + L.sc_off)[taun];
+            float2 kc[CT2], kn[CT2];
+            load_k(k_cur, kc);
+            load_k(k_nxt, kn);
+
+            // group B: c_t from St_{t-1} k_t, and its readout of token t-1
+            {
+                const float pkr = reduce_slots<NCL, RG>(pBk, lane);
+                broadcast_c(c_of(sct, load_v(stage, tau, rowB), pkr), ccB);
+                if constexpr (READOUT) {
+                    const float pqr = reduce_slots<NCL, RG>(pBq, lane);
+                    if (o_lane && !TWIN && tg > 0) store_o(o_t - o_step, rowB, scp.x * pqr);
+                }
             }
-            if (fl & FLAG_DUMP) {
-                const int slot = p.ckpts[fl >> FLAG_INDEX_SHIFT].slot;
-                store_state(p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state, 0);
+            // group A: token t
+            float pAk[RG], pAq[RG];
+            group_pass(0, ccA, kc, kn, q_cur, pAk, pAq);
+            // group A: c_{t+1} and its readout of token t (issued between group B's FMAs)
+            {
+                const float pkr = reduce_slots<NCL, RG>(pAk, lane);
+                broadcast_c(c_of(scn, load_v(nst, taun, rowA), pkr), ccA);
+                if constexpr (READOUT) {
+                    const float pqr = reduce_slots<NCL, RG>(pAq, lane);
+                    if (o_lane) store_o(o_t, rowA, sct.x * pqr);
+                }
             }
-        }
-        if (has_next) {
-            broadcast_c(scn.y * vv - scn.z * pkr, creg);
+            // group B: token t
+            group_pass(1, ccB, kc, kn, q_cur, pBk, pBq);
+
+            const uint32_t fl = __float_as_uint(sct.w);
+            if (fl & FLAG_RENORM) {
+                const float2 ss = make_float2(sct.x, sct.x);
 #pragma unroll
-            for (int jj = 0; jj < CT2; ++jj) kc[jj] = kn[jj];
+                for (int i = 0; i < RT; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < CT2; ++jj) S[i][jj] = __fmul2_rn(S[i][jj], ss);
+                if (has_next) restart(k_nxt, scn, nst, taun);
+                if (fl & FLAG_DUMP) {
+                    const int slot = p.ckpts[fl >> FLAG_INDEX_SHIFT].slot;
+                    store_state(p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state, 0);
+                }
+            }
+            scp = sct;
             sct = scn;
         }
-        if (tau == kChunk - 1 || !has_next) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    // group B's readout of the last token
+    if constexpr (READOUT) {
+        if (ok && len > 0) {
+            const float pqr = reduce_slots<NCL, RG>(pBq, lane);
+            if (o_lane && !TWIN) store_o(o_head + (size_t)(len - 1) * (size_t)H * (size_t)dv, rowB, scp.x * pqr);
         }
     }
 

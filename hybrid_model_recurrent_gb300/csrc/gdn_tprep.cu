@@ -122,8 +122,9 @@ __device__ __forceinline__ uint32_t k_addr(uint32_t kbase, int row, int col) {
 
 __global__ void __launch_bounds__(kTpThreads, kTpBlocksPerSm) tprep_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char tp_raw[];
-    unsigned char* smem =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tp_raw) + 1023u) & ~uintptr_t(1023));
+    // aligned by pointer arithmetic on the shared array (not through an integer), so that the compiler keeps
+    // its address space and plain C++ accesses below compile to shared-memory loads and stores
+    unsigned char* smem = tp_raw + ((1024u - (smem_addr(tp_raw) & 1023u)) & 1023u);
     float* sl = reinterpret_cast<float*>(smem + TP_L);
     float* sy = reinterpret_cast<float*>(smem + TP_Y);
     float* sbg = reinterpret_cast<float*>(smem + TP_G);
