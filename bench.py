@@ -178,9 +178,10 @@ class ClockSampler:
 # the step
 # -------------------------------------------------------------------------------------------
 class Step:
-    def __init__(self, w: synth.Workload, device):
+    def __init__(self, w: synth.Workload, device, algo: str = "auto"):
         import hybrid_model_recurrent_gb300 as gdn
         self.gdn = gdn
+        self.algo = algo
         self.w = w
         self.dev = device
         self.cu = w.cu_seqlens
@@ -219,7 +220,7 @@ class Step:
         # the store the first step's resumes read (untimed)
         gdn.gdn_prefill_ckpt(self.inp.q, self.inp.k, self.inp.v, self.inp.alpha, self.inp.beta, self.cu,
                              ckpt_pos=self.ck, o=self.o, S_final=self.S_final, ckpt_states=self.ck_store[1],
-                             ws=self.ws)
+                             ws=self.ws, algo=algo)
 
     def units(self) -> int:
         return sum(self.tok_head.values())
@@ -241,7 +242,7 @@ class Step:
                    prefill=dict(ckpt_pos=self.ck, o=self.o, S_final=self.S_final, ckpt_states=write),
                    resume=dict(ckpt_states=read, ckpt_pos=self.ck, probes=self.probes, o_out=self.o_res,
                                S_out=self.S_out),
-                   replay=dict(m=self.m, r_num=REPLAY_R[0], r_den=REPLAY_R[1], S_hat=self.S_hat))
+                   replay=dict(m=self.m, r_num=REPLAY_R[0], r_den=REPLAY_R[1], S_hat=self.S_hat), algo=self.algo)
         if record is not None:
             e1.record(s)
             record.append((e0, e1))
@@ -252,11 +253,11 @@ class Step:
         g = self.gdn
         inp = inp or self.inp
         g.gdn_prefill_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, ckpt_pos=self.ck, o=self.o,
-                           S_final=self.S_final, ckpt_states=self.ckpt, ws=self.ws)
+                           S_final=self.S_final, ckpt_states=self.ckpt, ws=self.ws, algo=self.algo)
         g.gdn_resume_from_ckpt(inp.q, inp.k, inp.v, inp.alpha, inp.beta, self.cu, self.ckpt, self.ck, self.probes,
-                               o_out=self.o_res, S_out=self.S_out, ws=self.ws)
+                               o_out=self.o_res, S_out=self.S_out, ws=self.ws, algo=self.algo)
         g.gdn_tail_replay(None, inp.k, inp.v, inp.alpha, inp.beta, self.cu, self.m, *REPLAY_R, S_hat=self.S_hat,
-                          ws=self.ws)
+                          ws=self.ws, algo=self.algo)
 
     def outputs(self):
         return [self.o, self.S_final, self.ckpt, self.S_out, self.o_res[:self.resume_rows], self.S_hat]
@@ -610,7 +611,7 @@ def run_ours(args, ws, rank, local):
     init_dist(ws, "nccl")
     gdn.build()
     w = synth.workload(WORKLOAD, seed=rank)
-    step = Step(w, dev)
+    step = Step(w, dev, args.algo)
     gdn.clear_status(dev)
     for _ in range(max(args.warmup, 3)):
         step.run()
@@ -671,7 +672,7 @@ def run_ours(args, ws, rank, local):
     # The same steps as a serving loop runs them: step i's inputs go in on one stream while step i-1 computes
     # and step i-2's results come out on a third (two sets of device inputs and outputs, one pinned host set
     # each way); every step still copies all of its inputs in and all of its results out.
-    step2 = Step(w, dev)
+    step2 = Step(w, dev, args.algo)
     steps = (step, step2)
     fields = lambda x: (x.q, x.k, x.v, x.alpha, x.beta)
     dev_ins = (dev_in, synth.Inputs(*[torch.empty_like(t) for t in fields(dev_in)]))
@@ -740,18 +741,21 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": thr / 1e6, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": slowest / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 q/k/v/o)",
-            "data": "synthetic (seeded counter-based generator)", "config": config_dict(w, ws),
+            "data": "synthetic (seeded counter-based generator)",
+            "config": dict(config_dict(w, ws), **({} if args.algo == "auto" else {"algo": args.algo})),
             "e2e": {"value": e2e_thr / 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": "step i+1's inputs in and step i-1's results out overlap step i (3 streams)",
                     "serial_value": e2e_serial_thr / 1e6,
                     "steps": e2e_steps},
             "gpu_launches": step.launches_per_step * args.steps,
             "roofline": {"bound": "hbm",
-                         "kernel": "gdn_chunk_tc_kernel<bf16 out, readout>: the step's two launches side by side "
-                                   "(the prefill jobs; the resume and tail-replay jobs), bytes of both over the "
-                                   "step's span",
+                         "kernel": ("gdn_chunk_tc_kernel<bf16 out, readout>" if args.algo in ("auto", "chunked")
+                                    else f"the {args.algo} path") +
+                                   ": the step's two launches side by side (the prefill jobs; the resume and "
+                                   "tail-replay jobs), bytes of both over the step's span",
                          "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved_gbs / hbm_peak, "traffic": profile_traffic(),
+                         "frac": achieved_gbs / hbm_peak,
+                         "traffic": profile_traffic() if args.algo in ("auto", "chunked") else None,
                          "launch_ms": launch_ms, "algorithmic_bytes_per_launch": bytes_per_launch,
                          "launch_ms_is": "CUDA-event span of the gdn_step call on the step's stream (both launches)",
                          "algorithmic_bytes": {"prefill": bytes_pf, "resume": bytes_rs, "replay": bytes_rp,
@@ -786,6 +790,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--algo", choices=["auto", "chunked", "two_pass", "per_token"], default="auto",
+                    help="kernel the step's calls ask for (default: the library's choice, the tcgen05 chunked scan); "
+                         "the others are for profiling those kernels on the same step")
     ap.add_argument("--step-only", action="store_true",
                     help="time the step (and its three-call form) only: no placement, overlap, chunked-variant or "
                          "other-workload reports (a few GB on the device, for profiler captures)")
