@@ -12,10 +12,10 @@
 //    right, so the rows of a head split across lanes, warps and CTAs with no
 //    exchange.  A consumer warp owns 16 state rows ("slots"): lanes form 4 row
 //    groups of 8 column lanes, and a lane holds a 4-row x (d_k/8)-column register
-//    tile.  The dot products S k and S q reduce over the 8 column lanes with a
-//    reduce-scatter that leaves lanes 2s and 2s+1 of a group with slot s's sums.
-//    Two or more consumer warps share each SM sub-partition, hiding each other's
-//    per-token dependency chain.
+//    tile, whose rows form two groups of 2 run half a token apart.  The dot products
+//    S k and S q of a group reduce over the 8 column lanes with a reduce-scatter
+//    that leaves lanes 4s..4s+3 of a row group with slot s's sums.  Two consumer
+//    warps share each SM sub-partition, hiding each other's per-token chain.
 //  * The state is kept in a running scale: S = s * St.  With s_t = alpha_t s_{t-1}
 //    the update becomes St += c k^T with c = (beta/s_t) v - beta (St_{t-1} k), so
 //    each state element costs exactly three FMAs per token (update, S k, S q),
@@ -46,9 +46,10 @@ constexpr int kStages = 3;     // depth of the shared-memory ring
 constexpr int kMaxJobs = 256;  // jobs per launch (host splits larger batches)
 constexpr int kMaxCkpts = 1536;
 // A lane holds kRowSlots state rows x (d_k / kColLanes) columns; the rows split into two groups that run half
-// a token apart (see the consumer loop).  Shared memory delivers 32 floats a cycle to an SM and every float of
-// k or q a lane loads feeds one FMA per row it holds, so 4 rows keep the loads under the FMA time, and the 64
-// registers of a d_k = 128 tile leave room for 8 consumer warps (two per SM sub-partition) at 168 registers.
+// a token apart (see the consumer loop).  Shared memory serves a warp's broadcast 16-byte load in 2 cycles (64
+// floats a cycle to an SM, against 128 FMAs) and every float of k or q a lane loads feeds one FMA per row it
+// holds, so 4 rows keep the loads under the FMA time, and the 64 registers of a d_k = 128 tile leave room for
+// 8 consumer warps (two per SM sub-partition) at 168 registers.
 constexpr int kColLanes = 8;
 constexpr int kRowSlots = 4;
 constexpr int kMaxConsumerWarps = 8;
