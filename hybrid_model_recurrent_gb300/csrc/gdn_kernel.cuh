@@ -580,7 +580,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
     }
 
-    // Chunks of the stage ring outside, tokens inside: per token only pointer steps, no index division.
+    // Chunks of the stage ring outside, tokens inside: per token only pointer steps, no index division.  A chunk
+    // runs as two segments, tokens 0 .. n-2 (the next token is in this stage) and token n-1 (the next token, if
+    // any, is the first of the next stage, waited for in between), and a renormalising token leaves the token loop:
+    // the wait, the renormalisation, the restart and the checkpoint dump stay out of the loop body, whose code the
+    // compiler then schedules on its own (measured: the same loop with that code inside it ran 1.4x longer).
     OutT* o_t = o_head;   // output row of the current token
     const size_t o_step = (size_t)H * (size_t)dv;
     int tg = 0;
@@ -591,66 +595,83 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         const unsigned char* stage_n = smem + (size_t)stn * L.bytes;
         const int n = min(kChunk, len - c * kChunk);
         const bool more = c + 1 < nchunks;
-        for (int tau = 0; tau < n; ++tau, ++tg, o_t += o_step) {
-            const bool edge = tau == n - 1;   // the next token, if any, is the next stage's first
-            if (edge && more) {
+        int tau = 0;
+        for (int seg = 0; seg < 2; ++seg) {
+            const int tau_end = seg == 0 ? n - 1 : n;
+            if (seg == 1 && more) {
                 if (!warp_wait(&full[stn], (uint32_t)(((c + 1) / kStages) & 1), limit)) {
                     ok = false;
                     break;
                 }
             }
-            const bool has_next = !edge || more;
-            const unsigned char* nst = edge ? stage_n : stage;
-            const int taun = edge ? 0 : tau + 1;
-            // k of the next token (the last token dots with its own k; those sums are never used).  Past the last
-            // token the next-token reads below stay inside the stage ring and are not used either.
-            const unsigned char* k_cur = stage + L.kf_off + (size_t)tau * DK * 4;
-            const unsigned char* k_nxt = has_next ? nst + L.kf_off + (size_t)taun * DK * 4 : k_cur;
-            const unsigned char* q_cur = stage + L.qf_off + (size_t)tau * DK * 4;
-            const float4 scn = reinterpret_cast<const float4*>(nst + L.sc_off)[taun];
-            float2 kc[CT2], kn[CT2];
-            load_k(k_cur, kc);
-            load_k(k_nxt, kn);
+            const unsigned char* nst = seg == 0 ? stage : stage_n;   // stage of the next token
+            const bool has_next = seg == 0 || more;                 // the next token exists
+            while (tau < tau_end) {
+                int tau_r = -1;   // a token after which the state renormalises
+                for (; tau < tau_end; ++tau, ++tg, o_t += o_step) {
+                    const int taun = seg == 0 ? tau + 1 : 0;
+                    // k of the next token (the last token dots with its own k; those sums are never used).  Past
+                    // the last token the next-token reads below stay inside the stage ring and are not used either.
+                    const unsigned char* k_cur = stage + L.kf_off + (size_t)tau * DK * 4;
+                    const unsigned char* k_nxt = has_next ? nst + L.kf_off + (size_t)taun * DK * 4 : k_cur;
+                    const unsigned char* q_cur = stage + L.qf_off + (size_t)tau * DK * 4;
+                    const float4 scn = reinterpret_cast<const float4*>(nst + L.sc_off)[taun];
+                    float2 kc[CT2], kn[CT2];
+                    load_k(k_cur, kc);
+                    load_k(k_nxt, kn);
 
-            // group B: c_t from St_{t-1} k_t, and its readout of token t-1
-            {
-                const float pkr = reduce_slots<NCL, RG>(pBk, lane);
-                broadcast_c(c_of(sct, load_v(stage, tau, rowB), pkr), ccB);
-                if constexpr (READOUT) {
-                    const float pqr = reduce_slots<NCL, RG>(pBq, lane);
-                    if (o_lane && !TWIN && tg > 0) store_o(o_t - o_step, rowB, scp.x * pqr);
-                }
-            }
-            // group A: token t
-            float pAk[RG], pAq[RG];
-            group_pass(0, ccA, kc, kn, q_cur, pAk, pAq);
-            // group A: c_{t+1} and its readout of token t (issued between group B's FMAs)
-            {
-                const float pkr = reduce_slots<NCL, RG>(pAk, lane);
-                broadcast_c(c_of(scn, load_v(nst, taun, rowA), pkr), ccA);
-                if constexpr (READOUT) {
-                    const float pqr = reduce_slots<NCL, RG>(pAq, lane);
-                    if (o_lane) store_o(o_t, rowA, sct.x * pqr);
-                }
-            }
-            // group B: token t
-            group_pass(1, ccB, kc, kn, q_cur, pBk, pBq);
+                    // group B: c_t from St_{t-1} k_t, and its readout of token t-1
+                    {
+                        const float pkr = reduce_slots<NCL, RG>(pBk, lane);
+                        broadcast_c(c_of(sct, load_v(stage, tau, rowB), pkr), ccB);
+                        if constexpr (READOUT) {
+                            const float pqr = reduce_slots<NCL, RG>(pBq, lane);
+                            if (o_lane && !TWIN && tg > 0) store_o(o_t - o_step, rowB, scp.x * pqr);
+                        }
+                    }
+                    // group A: token t
+                    float pAk[RG], pAq[RG];
+                    group_pass(0, ccA, kc, kn, q_cur, pAk, pAq);
+                    // group A: c_{t+1} and its readout of token t (issued between group B's FMAs)
+                    {
+                        const float pkr = reduce_slots<NCL, RG>(pAk, lane);
+                        broadcast_c(c_of(scn, load_v(nst, taun, rowA), pkr), ccA);
+                        if constexpr (READOUT) {
+                            const float pqr = reduce_slots<NCL, RG>(pAq, lane);
+                            if (o_lane) store_o(o_t, rowA, sct.x * pqr);
+                        }
+                    }
+                    // group B: token t
+                    group_pass(1, ccB, kc, kn, q_cur, pBk, pBq);
 
-            const uint32_t fl = __float_as_uint(sct.w);
-            if (fl & FLAG_RENORM) {
-                const float2 ss = make_float2(sct.x, sct.x);
+                    const bool renorm = (__float_as_uint(sct.w) & FLAG_RENORM) != 0u;
+                    scp = sct;
+                    sct = scn;
+                    if (renorm) {
+                        tau_r = tau;
+                        ++tau;
+                        ++tg;
+                        o_t += o_step;
+                        break;
+                    }
+                }
+                if (tau_r >= 0) {
+                    // after token tau_r (its scalars now in scp, the next token's in sct): St <- s St, then the
+                    // next token's c and partial sums from the renormalised state, and a checkpoint if one is due
+                    const uint32_t fl = __float_as_uint(scp.w);
+                    const float2 ss = make_float2(scp.x, scp.x);
 #pragma unroll
-                for (int i = 0; i < RT; ++i)
+                    for (int i = 0; i < RT; ++i)
 #pragma unroll
-                    for (int jj = 0; jj < CT2; ++jj) S[i][jj] = __fmul2_rn(S[i][jj], ss);
-                if (has_next) restart(k_nxt, scn, nst, taun);
-                if (fl & FLAG_DUMP) {
-                    const int slot = p.ckpts[fl >> FLAG_INDEX_SHIFT].slot;
-                    store_state(p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state, 0);
+                        for (int jj = 0; jj < CT2; ++jj) S[i][jj] = __fmul2_rn(S[i][jj], ss);
+                    const int taun_r = seg == 0 ? tau_r + 1 : 0;
+                    if (has_next) restart(nst + L.kf_off + (size_t)taun_r * DK * 4, sct, nst, taun_r);
+                    if (fl & FLAG_DUMP) {
+                        const int slot = p.ckpts[fl >> FLAG_INDEX_SHIFT].slot;
+                        store_state(p.ckpt_states + (size_t)slot * (size_t)H * (size_t)dv * DK + head_state, 0);
+                    }
                 }
             }
-            scp = sct;
-            sct = scn;
         }
         if (!ok) break;
         __syncwarp();
