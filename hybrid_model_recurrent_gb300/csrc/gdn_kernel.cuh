@@ -54,6 +54,10 @@ constexpr int kColLanes = 8;
 constexpr int kRowSlots = 4;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kSlotsPerWarp = (32 / kColLanes) * kRowSlots;   // state rows (slots) held by one consumer warp
+// With d_k = 128 the warps stage their own inputs (see the kernel): 8 warps of 64-register tiles then may use
+// 255 registers, where a producer warp as a ninth would cap them at 168 (measured: -20 % time).  The smaller
+// sizes keep a producer warp (at most 4 + 1 warps, already under no cap), which spares them the staging work.
+__host__ __device__ constexpr bool staging_in_warps(int dk) { return dk == 128; }
 constexpr float kRenormFloor = 0x1p-32f;
 // Bound of the wait for this CTA's own copies in flight before it exits (independent of the
 // user's wait limit, so that even a tiny limit never lets a CTA leave with a copy pending).
@@ -166,6 +170,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 // Wait for the phase of `parity` to complete, for at most limit_ns.  Called by
 // all 32 lanes of a warp; the warp agrees on the outcome.
+// orders this thread's (and, after a barrier, the CTA's) generic-proxy shared-memory accesses before later
+// async-proxy ones (TMA copies into the same bytes)
+__device__ __forceinline__ void proxy_fence_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
@@ -256,16 +263,17 @@ __host__ __device__ inline StageLayout stage_layout(int dk, int in_bytes, int ro
     L.tx_bytes = kr * (readout ? 2u : 1u) + vb;
     return L;
 }
-// barriers: raw[kStages], full[kStages], empty[kStages]
+// after the stages: barriers raw[kStages] and full[kStages], the scan carry (8 B), done counters
+// [kStages] and the issued count (4 B each), then up to 127 B of alignment of the base
 __host__ __device__ inline uint32_t smem_bytes(int dk, int in_bytes, int rows, bool readout) {
-    return stage_layout(dk, in_bytes, rows, readout).bytes * kStages + 3u * kStages * 8u + 128u;
+    return stage_layout(dk, in_bytes, rows, readout).bytes * kStages + 256u + 128u;
 }
 
 // ------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------
 template <int DK, bool IN_BF16, bool OUT_BF16, bool READOUT, bool TWIN>
-__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
+__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK) ? 0 : 1)), 1)
     gdn_scan_kernel(const __grid_constant__ Params p) {
     constexpr int ES = IN_BF16 ? 2 : 4;
     constexpr int NCL = kColLanes;           // column lanes per row group
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     static_assert(CH4 >= 1 && CT % 4 == 0, "lane tile");
     static_assert(NRG * RT == kSlotsPerWarp, "slots per warp");
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
+    constexpr bool FOLD = staging_in_warps(DK);   // the warps stage their inputs themselves (no producer warp)
 
     // the 128-byte aligned base is formed by pointer arithmetic on the shared array (not through an integer),
     // so that the compiler keeps its address space and reads the stages with shared-memory loads
@@ -292,9 +301,13 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const StageLayout L = stage_layout(DK, ES, RB, READOUT);
-    uint64_t* rawb = reinterpret_cast<uint64_t*>(smem + L.bytes * kStages);
-    uint64_t* full = rawb + kStages;
-    uint64_t* empty = full + kStages;
+    uint64_t* rawb = reinterpret_cast<uint64_t*>(smem + L.bytes * kStages);   // [kStages] a chunk's copies landed
+    uint64_t* full = rawb + kStages;   // [kStages] a chunk widened and its scalars written
+    uint64_t* empty = full + kStages;  // [kStages] (with the producer warp) every warp done with a stage's chunk
+    float* carry_s = reinterpret_cast<float*>(empty + kStages);   // running scale after the last scanned chunk
+    int* carry_ck = reinterpret_cast<int*>(carry_s + 1);         // checkpoint cursor after it
+    int* done_cnt = carry_ck + 1;                                // [kStages] warps done with a stage's chunk
+    int* issued_sh = done_cnt + kStages;                         // chunks whose copies were issued
 
     const int per_job = p.H * p.ctas_per_head;
     const int job_idx = blockIdx.x / per_job;
@@ -311,110 +324,116 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&rawb[s], 1);
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], FOLD ? (uint32_t)nw : 1u);   // every warp, or the producer
             mbar_init(&empty[s], (uint32_t)nw);
+            done_cnt[s] = 0;
         }
+        *carry_s = 1.0f;
+        *carry_ck = p.jobs[job_idx].ck_begin;
+        *issued_sh = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
-    if (warp == nw) {
-        // ============================== producer warp ==============================
-        const size_t gate0 = (size_t)tok_begin * (size_t)H + (size_t)h;
-        const int ck_end = p.jobs[job_idx].ck_begin + p.jobs[job_idx].ck_count;
-        int ck_cur = p.jobs[job_idx].ck_begin;
-        float s_carry = 1.0f;
-        int issued = 0;
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int st = c % kStages;
-            if (p.stall_after >= 0 && c >= p.stall_after) break;   // testing hook (see Params)
-            if (c >= kStages && !warp_wait(&empty[st], (uint32_t)(((c / kStages) + 1) & 1), limit)) {
-                ok = false;
-                break;
-            }
-            unsigned char* stage = smem + (size_t)st * L.bytes;
-            uint64_t* landing = IN_BF16 ? &rawb[st] : &full[st];
-            if (lane == 0) {
-                // bf16: the landing barrier completes on the copies alone (one arrival
-                // here); fp32: the copies land on `full`, which the producer arrives
-                // on after publishing the scalars
-                if constexpr (IN_BF16)
-                    mbar_arrive_expect_tx(landing, L.tx_bytes);
-                else
-                    mbar_expect_tx(landing, L.tx_bytes);
-                const int t0 = (int)(tok_begin + (int64_t)c * kChunk);
-                tma_load_3d(stage + (IN_BF16 ? L.kr_off : L.kf_off), &p.tm_k, 0, h, t0, landing);
-                if (READOUT) tma_load_3d(stage + (IN_BF16 ? L.qr_off : L.qf_off), &p.tm_q, 0, h, t0, landing);
-                tma_load_3d(stage + L.v_off, &p.tm_v, rb * RB, h, t0, landing);
-            }
-            issued = c + 1;
-            const int base = c * kChunk;
-            const int tau = base + lane;
-            float a = 1.0f, b = 0.0f;
-            if (tau < len) {
-                a = __ldg(p.alpha + gate0 + (size_t)tau * (size_t)H);
-                b = __ldg(p.beta + gate0 + (size_t)tau * (size_t)H);
-            }
-            float a_look = 1.0f;
-            if (base + kChunk < len) a_look = __ldg(p.alpha + gate0 + (size_t)(base + kChunk) * (size_t)H);
-            uint32_t fl = 0;
-            while (ck_cur < ck_end && p.ckpts[ck_cur].pos <= base + kChunk) {
-                if (p.ckpts[ck_cur].pos - 1 == tau)
-                    fl = FLAG_DUMP | FLAG_RENORM | ((uint32_t)ck_cur << FLAG_INDEX_SHIFT);
-                ++ck_cur;
-            }
-            if (tau == len - 1) fl |= FLAG_RENORM;
-            // running scale, left to right (chunk-boundary independent)
-            float s = s_carry, my_s = 1.0f;
-            uint32_t my_fl = fl;
-#pragma unroll 4
-            for (int j = 0; j < kChunk; ++j) {
-                const float aj = __shfl_sync(0xffffffffu, a, j);
-                const float an_sh = __shfl_sync(0xffffffffu, a, (j + 1) & 31);
-                const uint32_t fj = __shfl_sync(0xffffffffu, fl, j);
-                const float an = (j + 1 < kChunk) ? an_sh : a_look;
-                s = s * aj;
-                const bool valid = base + j < len;
-                const bool ren =
-                    valid && ((fj & FLAG_RENORM) != 0u || (base + j + 1 < len && s * an < kRenormFloor));
-                if (lane == j) {
-                    my_s = s;
-                    my_fl = fj | (ren ? FLAG_RENORM : 0u);
-                }
-                if (ren) s = 1.0f;
-            }
-            s_carry = s;
-            const float b1 = __fdiv_rn(b, my_s);
-            reinterpret_cast<float4*>(stage + L.sc_off)[lane] = make_float4(my_s, b1, b, __uint_as_float(my_fl));
-            if constexpr (IN_BF16) {
-                // widen k (and q) to fp32 once for all consumer warps
-                if (!warp_wait(&rawb[st], (uint32_t)((c / kStages) & 1), limit)) {
+    if constexpr (!FOLD) {
+        if (warp == nw) {
+            // ============================== producer warp ==============================
+            const size_t gate0 = (size_t)tok_begin * (size_t)H + (size_t)h;
+            const int ck_end = p.jobs[job_idx].ck_begin + p.jobs[job_idx].ck_count;
+            int ck_cur = p.jobs[job_idx].ck_begin;
+            float s_carry = 1.0f;
+            int issued = 0;
+            bool ok = true;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c % kStages;
+                if (p.stall_after >= 0 && c >= p.stall_after) break;   // testing hook (see Params)
+                if (c >= kStages && !warp_wait(&empty[st], (uint32_t)(((c / kStages) + 1) & 1), limit)) {
                     ok = false;
-                    break;   // this chunk's copy stays accounted for by the drain below
+                    break;
                 }
-                constexpr int NV4 = kChunk * DK / 4;   // groups of 4 elements
-#pragma unroll 4
-                for (int g = lane; g < NV4; g += 32) {
-                    const uint2 w = reinterpret_cast<const uint2*>(stage + L.kr_off)[g];
-                    const float2 lo = bf16x2_to_float2(w.x), hi = bf16x2_to_float2(w.y);
-                    reinterpret_cast<float4*>(stage + L.kf_off)[g] = make_float4(lo.x, lo.y, hi.x, hi.y);
-                    if (READOUT) {
-                        const uint2 u = reinterpret_cast<const uint2*>(stage + L.qr_off)[g];
-                        const float2 ql = bf16x2_to_float2(u.x), qh = bf16x2_to_float2(u.y);
-                        reinterpret_cast<float4*>(stage + L.qf_off)[g] = make_float4(ql.x, ql.y, qh.x, qh.y);
+                unsigned char* stage = smem + (size_t)st * L.bytes;
+                uint64_t* landing = IN_BF16 ? &rawb[st] : &full[st];
+                if (lane == 0) {
+                    // bf16: the landing barrier completes on the copies alone (one arrival
+                    // here); fp32: the copies land on `full`, which the producer arrives
+                    // on after publishing the scalars
+                    if constexpr (IN_BF16)
+                        mbar_arrive_expect_tx(landing, L.tx_bytes);
+                    else
+                        mbar_expect_tx(landing, L.tx_bytes);
+                    const int t0 = (int)(tok_begin + (int64_t)c * kChunk);
+                    tma_load_3d(stage + (IN_BF16 ? L.kr_off : L.kf_off), &p.tm_k, 0, h, t0, landing);
+                    if (READOUT) tma_load_3d(stage + (IN_BF16 ? L.qr_off : L.qf_off), &p.tm_q, 0, h, t0, landing);
+                    tma_load_3d(stage + L.v_off, &p.tm_v, rb * RB, h, t0, landing);
+                }
+                issued = c + 1;
+                const int base = c * kChunk;
+                const int tau = base + lane;
+                float a = 1.0f, b = 0.0f;
+                if (tau < len) {
+                    a = __ldg(p.alpha + gate0 + (size_t)tau * (size_t)H);
+                    b = __ldg(p.beta + gate0 + (size_t)tau * (size_t)H);
+                }
+                float a_look = 1.0f;
+                if (base + kChunk < len) a_look = __ldg(p.alpha + gate0 + (size_t)(base + kChunk) * (size_t)H);
+                uint32_t fl = 0;
+                while (ck_cur < ck_end && p.ckpts[ck_cur].pos <= base + kChunk) {
+                    if (p.ckpts[ck_cur].pos - 1 == tau)
+                        fl = FLAG_DUMP | FLAG_RENORM | ((uint32_t)ck_cur << FLAG_INDEX_SHIFT);
+                    ++ck_cur;
+                }
+                if (tau == len - 1) fl |= FLAG_RENORM;
+                // running scale, left to right (chunk-boundary independent)
+                float s = s_carry, my_s = 1.0f;
+                uint32_t my_fl = fl;
+    #pragma unroll 4
+                for (int j = 0; j < kChunk; ++j) {
+                    const float aj = __shfl_sync(0xffffffffu, a, j);
+                    const float an_sh = __shfl_sync(0xffffffffu, a, (j + 1) & 31);
+                    const uint32_t fj = __shfl_sync(0xffffffffu, fl, j);
+                    const float an = (j + 1 < kChunk) ? an_sh : a_look;
+                    s = s * aj;
+                    const bool valid = base + j < len;
+                    const bool ren =
+                        valid && ((fj & FLAG_RENORM) != 0u || (base + j + 1 < len && s * an < kRenormFloor));
+                    if (lane == j) {
+                        my_s = s;
+                        my_fl = fj | (ren ? FLAG_RENORM : 0u);
+                    }
+                    if (ren) s = 1.0f;
+                }
+                s_carry = s;
+                const float b1 = __fdiv_rn(b, my_s);
+                reinterpret_cast<float4*>(stage + L.sc_off)[lane] = make_float4(my_s, b1, b, __uint_as_float(my_fl));
+                if constexpr (IN_BF16) {
+                    // widen k (and q) to fp32 once for all consumer warps
+                    if (!warp_wait(&rawb[st], (uint32_t)((c / kStages) & 1), limit)) {
+                        ok = false;
+                        break;   // this chunk's copy stays accounted for by the drain below
+                    }
+                    constexpr int NV4 = kChunk * DK / 4;   // groups of 4 elements
+    #pragma unroll 4
+                    for (int g = lane; g < NV4; g += 32) {
+                        const uint2 w = reinterpret_cast<const uint2*>(stage + L.kr_off)[g];
+                        const float2 lo = bf16x2_to_float2(w.x), hi = bf16x2_to_float2(w.y);
+                        reinterpret_cast<float4*>(stage + L.kf_off)[g] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                        if (READOUT) {
+                            const uint2 u = reinterpret_cast<const uint2*>(stage + L.qr_off)[g];
+                            const float2 ql = bf16x2_to_float2(u.x), qh = bf16x2_to_float2(u.y);
+                            reinterpret_cast<float4*>(stage + L.qf_off)[g] = make_float4(ql.x, ql.y, qh.x, qh.y);
+                        }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[st]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[st]);
+            // never leave with copies in flight into this CTA's shared memory
+            for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
+                warp_wait(IN_BF16 ? &rawb[c % kStages] : &full[c % kStages], (uint32_t)((c / kStages) & 1),
+                          limit > kDrainLimitNs ? limit : kDrainLimitNs);
+            if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
+            return;
         }
-        // never leave with copies in flight into this CTA's shared memory
-        for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
-            warp_wait(IN_BF16 ? &rawb[c % kStages] : &full[c % kStages], (uint32_t)((c / kStages) & 1),
-                      limit > kDrainLimitNs ? limit : kDrainLimitNs);
-        if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
-        return;
     }
 
     // ================================ consumer warps ===============================
@@ -564,6 +583,116 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         dot_group(1, ktok, pBk);
     };
 
+    // ---- input staging by the warps themselves (no producer warp: a ninth warp would cap every thread at 168
+    //      registers, which costs the token loop ~20 %).  Chunk k's k, q, v tiles are copied by TMA into stage
+    //      k % 3; the warp that finishes chunk k - 3 last issues them.  At the start of chunk k - 1 every warp
+    //      prepares chunk k: it waits for the copies, widens its share of bf16 k and q to fp32, and warp k % nw
+    //      also writes the chunk's per-token scalars (the running scale s_t, beta_t / s_t, beta_t and the
+    //      renormalisation / checkpoint flags, left to right from the carry of chunk k - 1); each warp then
+    //      arrives on the chunk's `full` barrier, which every warp waits for before the last token of chunk
+    //      k - 1 reads chunk k's first token.  No barrier of the whole CTA: a warp that is slower at one chunk
+    //      holds the others back only through the stage ring. ----
+    const size_t gate0 = (size_t)tok_begin * (size_t)H + (size_t)h;
+    const int ck_end = p.jobs[job_idx].ck_begin + p.jobs[job_idx].ck_count;
+    auto issue = [&](int k) {   // one thread
+        if (p.stall_after >= 0 && k >= p.stall_after) return;   // testing hook (see Params)
+        const int s = k % kStages;
+        unsigned char* stage = smem + (size_t)s * L.bytes;
+        proxy_fence_shared();   // the warps' reads of this stage (chunk k - 3) come before the copies' writes
+        mbar_arrive_expect_tx(&rawb[s], L.tx_bytes);
+        const int t0 = (int)(tok_begin + (int64_t)k * kChunk);
+        tma_load_3d(stage + (IN_BF16 ? L.kr_off : L.kf_off), &p.tm_k, 0, h, t0, &rawb[s]);
+        if (READOUT) tma_load_3d(stage + (IN_BF16 ? L.qr_off : L.qf_off), &p.tm_q, 0, h, t0, &rawb[s]);
+        tma_load_3d(stage + L.v_off, &p.tm_v, rb * RB, h, t0, &rawb[s]);
+        atomicMax(issued_sh, k + 1);
+    };
+    // this warp's gates for the next chunk it scans (chunk k with k % nw == warp), loaded nw chunks ahead
+    float ga = 1.f, gb = 0.f, gal = 1.f;
+    auto load_gates = [&](int k) {
+        const int base = k * kChunk, tau = base + lane;
+        ga = 1.f;
+        gb = 0.f;
+        if (tau < len) {
+            ga = __ldg(p.alpha + gate0 + (size_t)tau * (size_t)H);
+            gb = __ldg(p.beta + gate0 + (size_t)tau * (size_t)H);
+        }
+        gal = 1.f;
+        if (base + kChunk < len) gal = __ldg(p.alpha + gate0 + (size_t)(base + kChunk) * (size_t)H);
+    };
+    auto prepare = [&](int k) -> bool {
+        const int s = k % kStages;
+        unsigned char* stage = smem + (size_t)s * L.bytes;
+        if (!warp_wait(&rawb[s], (uint32_t)((k / kStages) & 1), limit)) return false;
+        if constexpr (IN_BF16) {
+            constexpr int NV4 = kChunk * DK / 4;   // groups of 4 elements
+#pragma unroll 2
+            for (int g = warp * 32 + lane; g < NV4; g += 32 * nw) {
+                const uint2 w = reinterpret_cast<const uint2*>(stage + L.kr_off)[g];
+                const float2 lo = bf16x2_to_float2(w.x), hi = bf16x2_to_float2(w.y);
+                reinterpret_cast<float4*>(stage + L.kf_off)[g] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                if (READOUT) {
+                    const uint2 u = reinterpret_cast<const uint2*>(stage + L.qr_off)[g];
+                    const float2 ql = bf16x2_to_float2(u.x), qh = bf16x2_to_float2(u.y);
+                    reinterpret_cast<float4*>(stage + L.qf_off)[g] = make_float4(ql.x, ql.y, qh.x, qh.y);
+                }
+            }
+        }
+        if (k % nw == warp) {
+            // the per-token scalars, left to right from the carry (chunk-boundary independent); the carry was
+            // written by the scan of chunk k - 1, which this warp has seen complete through that chunk's `full`
+            const int base = k * kChunk;
+            const int tau = base + lane;
+            int ck_cur = *carry_ck;
+            uint32_t fl = 0;
+            while (ck_cur < ck_end && p.ckpts[ck_cur].pos <= base + kChunk) {
+                if (p.ckpts[ck_cur].pos - 1 == tau) fl = FLAG_DUMP | FLAG_RENORM | ((uint32_t)ck_cur << FLAG_INDEX_SHIFT);
+                ++ck_cur;
+            }
+            if (tau == len - 1) fl |= FLAG_RENORM;
+            float sc_run = *carry_s, my_s = 1.0f;
+            uint32_t my_fl = fl;
+#pragma unroll 4
+            for (int j = 0; j < kChunk; ++j) {
+                const float aj = __shfl_sync(0xffffffffu, ga, j);
+                const float an_sh = __shfl_sync(0xffffffffu, ga, (j + 1) & 31);
+                const uint32_t fj = __shfl_sync(0xffffffffu, fl, j);
+                const float an = (j + 1 < kChunk) ? an_sh : gal;
+                sc_run = sc_run * aj;
+                const bool valid = base + j < len;
+                const bool ren =
+                    valid && ((fj & FLAG_RENORM) != 0u || (base + j + 1 < len && sc_run * an < kRenormFloor));
+                if (lane == j) {
+                    my_s = sc_run;
+                    my_fl = fj | (ren ? FLAG_RENORM : 0u);
+                }
+                if (ren) sc_run = 1.0f;
+            }
+            const float b1 = __fdiv_rn(gb, my_s);
+            reinterpret_cast<float4*>(stage + L.sc_off)[lane] = make_float4(my_s, b1, gb, __uint_as_float(my_fl));
+            if (lane == 0) {
+                *carry_s = sc_run;
+                *carry_ck = ck_cur;
+            }
+            if (k + nw < nchunks) load_gates(k + nw);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+        return true;
+    };
+    // this warp is done with chunk c: the last of the warps hands its stage to chunk c + 3
+    auto release = [&](int c) {
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const int s = c % kStages;
+            if (atomicAdd(&done_cnt[s], 1) == nw - 1) {
+                atomicExch(&done_cnt[s], 0);
+                __threadfence_block();
+                if (c + kStages < nchunks) issue(c + kStages);
+            }
+        }
+    };
+
     bool ok = true;
     float4 sct = make_float4(1.f, 0.f, 0.f, 0.f);   // scalars of the current token
     float4 scp = sct;                               // scalars of the token before
@@ -573,7 +702,13 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         pBk[i] = pBq[i] = 0.f;
     }
     if (len > 0) {
-        ok = warp_wait(&full[0], 0u, limit);
+        if constexpr (FOLD) {
+            if (threadIdx.x == 0)
+                for (int k = 0; k < kStages && k < nchunks; ++k) issue(k);
+            if (warp < nchunks) load_gates(warp);   // the first chunk each warp scans
+            ok = prepare(0);
+        }
+        ok = ok && warp_wait(&full[0], 0u, limit);
         if (ok) {
             sct = reinterpret_cast<const float4*>(smem + L.sc_off)[0];
             restart(smem + L.kf_off, sct, smem, 0);
@@ -595,6 +730,12 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         const unsigned char* stage_n = smem + (size_t)stn * L.bytes;
         const int n = min(kChunk, len - c * kChunk);
         const bool more = c + 1 < nchunks;
+        if constexpr (FOLD) {
+            if (more && !prepare(c + 1)) {
+                ok = false;
+                break;
+            }
+        }
         int tau = 0;
         for (int seg = 0; seg < 2; ++seg) {
             const int tau_end = seg == 0 ? n - 1 : n;
@@ -674,8 +815,12 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
             }
         }
         if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        if constexpr (FOLD) {
+            release(c);
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
     }
     // group B's readout of the last token
     if constexpr (READOUT) {
@@ -685,6 +830,16 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1), 1)
         }
     }
 
+    // never leave with copies in flight into this CTA's shared memory (after a wait ran out, copies of chunks
+    // not prepared may still be landing): every warp is out of its loops, then warp 0 waits for the last ones
+    if constexpr (FOLD) {
+        __syncthreads();   // (with the producer warp, that warp drains its own copies)
+        if (warp == 0) {
+        const int iss = *issued_sh;
+        for (int k = iss > kStages ? iss - kStages : 0; k < iss; ++k)
+            warp_wait(&rawb[k % kStages], (uint32_t)((k / kStages) & 1), limit > kDrainLimitNs ? limit : kDrainLimitNs);
+        }
+    }
     if (!ok) {
         if (lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
         return;
@@ -723,7 +878,7 @@ cudaError_t launch_scan(const Params& p, int grid, size_t smem, cudaStream_t str
     static std::atomic<int> optin[kMaxOptinDevices];
     cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), (int)smem, optin);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 32 * (p.nw + 1), smem, stream>>>(p);
+    kern<<<grid, 32 * (p.nw + (staging_in_warps(DK) ? 0 : 1)), smem, stream>>>(p);
     return cudaGetLastError();
 }
 
