@@ -111,6 +111,8 @@ def test_tiny_prefill_resume_replay():
     (128, 128, torch.float32, torch.float32, "auto"),
     (32, 32, torch.bfloat16, torch.float32, "auto"), (128, 64, torch.bfloat16, torch.float32, "auto"),
     (64, 128, torch.float32, torch.bfloat16, "auto"), (32, 128, torch.bfloat16, torch.bfloat16, "auto"),
+    # d_k = 128 on the per-token path with 2 and 4 warps (the warps stage their own inputs)
+    (128, 32, torch.bfloat16, torch.bfloat16, "per_token"), (128, 64, torch.float32, torch.float32, "per_token"),
 ])
 def test_ragged_prefill_with_initial_state(dk, dv, dtype, out, algo):
     lens = [100, 37, 0, 300, 1]
@@ -141,7 +143,8 @@ def test_ragged_prefill_with_initial_state(dk, dv, dtype, out, algo):
 
 
 @pytest.mark.parametrize("dk,dv,algo", [(128, 128, "per_token"), (128, 128, "chunked"), (128, 128, "chunked_mma"),
-                                        (128, 128, "two_pass"), (64, 32, "auto")])
+                                        (128, 128, "two_pass"), (64, 32, "auto"), (128, 64, "per_token"),
+                                        (128, 32, "per_token")])
 def test_ragged_replay_twin_and_readout(dk, dv, algo):
     lens = [200, 71, 5, 64]
     H = 4
