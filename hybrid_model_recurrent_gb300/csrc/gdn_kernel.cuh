@@ -19,16 +19,19 @@
 //  * The state is kept in a running scale: S = s * St.  With s_t = alpha_t s_{t-1}
 //    the update becomes St += c k^T with c = (beta/s_t) v - beta (St_{t-1} k), so
 //    each state element costs exactly three FMAs per token (update, S k, S q),
-//    issued as packed fp32x2 FMAs.  The producer warp computes s_t and beta/s_t
+//    issued as packed fp32x2 FMAs.  The input staging computes s_t and beta/s_t
 //    per token (sequential left-to-right product) and schedules renormalisation
 //    (St *= s, s = 1) whenever the scale would fall below 2^-32, at every
 //    checkpoint and after the last token, so dumps and results are plain states
 //    and the arithmetic after a checkpoint does not depend on the path before it.
-//  * One producer warp stages k, q, v tiles of 32 tokens with TMA into a 3-deep
-//    shared-memory ring guarded by mbarriers, widens bf16 k and q to fp32 once
-//    per CTA (consumers then read fp32 with conflict-free broadcast loads) and
-//    publishes the per-token scalars.  Every wait is bounded by a wall-clock
-//    limit; on expiry the kernel records the device status and returns.
+//  * k, q, v tiles of 32 tokens arrive by TMA in a 3-deep shared-memory ring
+//    guarded by mbarriers; bf16 k and q are widened to fp32 once per CTA (then
+//    read with conflict-free broadcast loads) and the per-token scalars are
+//    published beside them.  With d_k < 128 a producer warp does this; with
+//    d_k = 128 the warps do it themselves, a share each (a producer as a ninth
+//    warp would cap every thread at 168 registers).  Every wait is bounded by a
+//    wall-clock limit; on expiry the kernel records the device status and
+//    returns.
 #pragma once
 
 #include <cuda.h>
@@ -583,9 +586,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
         dot_group(1, ktok, pBk);
     };
 
-    // ---- input staging by the warps themselves (no producer warp: a ninth warp would cap every thread at 168
-    //      registers, which costs the token loop ~20 %).  Chunk k's k, q, v tiles are copied by TMA into stage
-    //      k % 3; the warp that finishes chunk k - 3 last issues them.  At the start of chunk k - 1 every warp
+    // ---- (d_k = 128) input staging by the warps themselves (no producer warp: a ninth warp would cap every
+    //      thread at 168 registers, which costs the token loop ~20 %).  Chunk k's k, q, v tiles are copied by TMA
+    //      into stage k % 3; the warp that finishes chunk k - 3 last issues them.  At the start of chunk k - 1 every warp
     //      prepares chunk k: it waits for the copies, widens its share of bf16 k and q to fp32, and warp k % nw
     //      also writes the chunk's per-token scalars (the running scale s_t, beta_t / s_t, beta_t and the
     //      renormalisation / checkpoint flags, left to right from the carry of chunk k - 1); each warp then
