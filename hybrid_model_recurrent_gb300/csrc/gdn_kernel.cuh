@@ -211,28 +211,29 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Reduce over the NCL column lanes of a row group.  On entry v[i] is this lane's partial sum for slot i
-// (RT slots); on exit the return value is the full sum of slot cl / (NCL / RT), held by the NCL / RT lanes
-// of the group with that quotient.  Each round of the reduce-scatter halves the slots a lane carries (the
-// lanes with the round's bit set keep the upper half); the lanes left sharing a slot then add up.
-template <int NCL, int RT>
-__device__ __forceinline__ float reduce_slots(float (&v)[RT], int lane) {
-    static_assert(NCL >= RT && (NCL & (NCL - 1)) == 0 && (RT & (RT - 1)) == 0, "lane split");
-    int step = NCL / 2;
-#pragma unroll
-    for (int n = RT; n > 1; n /= 2, step /= 2) {
-        const bool up = (lane & step) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            const float send = up ? v[i] : v[i + n / 2];
-            const float keep = up ? v[i + n / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
-        }
+// Sum over the NCL column lanes of a row group of a group's two per-row partial sums v[0], v[1].  The lanes
+// with bit NCL / 2 set end up with slot 1's sum, the others with slot 0's: the first round keeps one sum and
+// sends the other to the lane NCL / 2 away, then the lanes that share a slot add up.  With SWAPPED the caller
+// already holds its own slot's sum in v[0] and no select is needed; both forms add the same operands in the
+// same order.
+template <int NCL, bool SWAPPED>
+__device__ __forceinline__ float reduce_pair(float (&v)[2], int lane) {
+    float keep = v[0], send = v[1];
+    if constexpr (!SWAPPED) {
+        const bool up = (lane & (NCL / 2)) != 0;
+        send = up ? v[0] : v[1];
+        keep = up ? v[1] : v[0];
     }
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, NCL / 2);
 #pragma unroll
-    for (; step >= 1; step /= 2) v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], step);
+    for (int step = NCL / 4; step >= 1; step /= 2) v[0] = v[0] + __shfl_xor_sync(0xffffffffu, v[0], step);
     return v[0];
 }
+
+// Whether a lane holds the two rows of each group in the order "its own slot first" (see the consumer setup).
+// This removes the selects from every reduction; measured on GB300 it pays at d_k = 64 and 32 (6-7 % per
+// token) but costs 4 % at d_k = 128, where the loop sits at the register limit.
+__host__ __device__ constexpr bool swapped_rows(int dk) { return dk != 128; }
 
 // Shared-memory layout of one pipeline stage.
 //   kf, qf : [kChunk][dk] fp32, read by the consumers
@@ -448,17 +449,29 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     const int rg = lane / NCL;
     const int row0 = warp * WR + rg * HALF;                              // CTA row of this group's slot 0
     const int gslot = cl / LPG;                                          // slot (within a group) of this lane's sums
+    // With swapped_rows(DK) the lanes whose sums end up in slot 1 of a group hold the group's two rows in
+    // swapped registers, so that every lane's first reduction round keeps register 0 and sends register 1:
+    // register i of group g then holds slot g * RG + (i ^ gslot) (else slot i).
+    static_assert(RG == 2 && LPG == NCL / 2 && (!TWIN || HALF == RG),
+                  "two slots per group, reduced over the column lanes; the twin form's groups are its two states");
+    constexpr bool SWAP = swapped_rows(DK);
+    const int rswap = SWAP ? gslot : 0;
+    auto slot_of = [&](int i) {
+        if constexpr (SWAP) return (i / RG) * RG + ((i % RG) ^ rswap);
+        else return i;
+    };
+    auto reduce_group = [&](float (&v)[RG]) { return reduce_pair<NCL, SWAP>(v, lane); };
     const int rowA = row0 + gslot;                                       // CTA-relative real rows of those slots
     const int rowB = row0 + (TWIN ? gslot : RG + gslot);
     const int grow_base = rb * RB + row0;                                // head row of slot 0
     const size_t head_state = (size_t)h * (size_t)dv * DK;
 
-    // state tile: S[i][2*j4 + e] holds columns 4*(cl + 8*j4) + 2*e .. +1 of slot i
+    // state tile: S[i][2*j4 + e] holds columns 4*(cl + 8*j4) + 2*e .. +1 of slot slot_of(i)
     float2 S[RT][CT2];
 #pragma unroll
     for (int i = 0; i < RT; ++i) {
-        const int state = TWIN ? (i / HALF) : 0;
-        const int grow = grow_base + (TWIN ? (i % HALF) : i);
+        const int state = TWIN ? i / RG : 0;                             // the twin form's group g is state g
+        const int grow = grow_base + (TWIN ? slot_of(i) % RG : slot_of(i));
         const float* src = state == 0 ? p.jobs[job_idx].s0 : p.jobs[job_idx].s0_twin;
 #pragma unroll
         for (int j4 = 0; j4 < CH4; ++j4) {
@@ -508,7 +521,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
         const int grp = lane & ~(NCL - 1);
 #pragma unroll
         for (int i = 0; i < RG; ++i) {
-            const float c = __shfl_sync(0xffffffffu, c_mine, grp | (i * LPG));
+            const float c = __shfl_sync(0xffffffffu, c_mine, grp | ((i ^ rswap) * LPG));
             cc[i] = make_float2(c, c);
         }
     };
@@ -552,8 +565,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     auto store_state = [&](float* dst_head, int which) {
 #pragma unroll
         for (int i = 0; i < RT; ++i) {
-            if ((TWIN ? (i / HALF) : 0) != which) continue;
-            const int grow = grow_base + (TWIN ? (i % HALF) : i);
+            if ((TWIN ? i / RG : 0) != which) continue;
+            const int grow = grow_base + (TWIN ? slot_of(i) % RG : slot_of(i));
 #pragma unroll
             for (int j4 = 0; j4 < CH4; ++j4) {
                 const float2 a0 = S[i][2 * j4 + 0], a1 = S[i][2 * j4 + 1];
@@ -581,7 +594,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     auto restart = [&](const unsigned char* ktok, const float4& sc, const unsigned char* stg, int tau) {
         float pk[RG];
         dot_group(0, ktok, pk);
-        const float pkr = reduce_slots<NCL, RG>(pk, lane);
+        const float pkr = reduce_group(pk);
         broadcast_c(c_of(sc, load_v(stg, tau, rowA), pkr), ccA);
         dot_group(1, ktok, pBk);
     };
@@ -766,10 +779,10 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
 
                     // group B: c_t from St_{t-1} k_t, and its readout of token t-1
                     {
-                        const float pkr = reduce_slots<NCL, RG>(pBk, lane);
+                        const float pkr = reduce_group(pBk);
                         broadcast_c(c_of(sct, load_v(stage, tau, rowB), pkr), ccB);
                         if constexpr (READOUT) {
-                            const float pqr = reduce_slots<NCL, RG>(pBq, lane);
+                            const float pqr = reduce_group(pBq);
                             if (o_lane && !TWIN && tg > 0) store_o(o_t - o_step, rowB, scp.x * pqr);
                         }
                     }
@@ -778,10 +791,10 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
                     group_pass(0, ccA, kc, kn, q_cur, pAk, pAq);
                     // group A: c_{t+1} and its readout of token t (issued between group B's FMAs)
                     {
-                        const float pkr = reduce_slots<NCL, RG>(pAk, lane);
+                        const float pkr = reduce_group(pAk);
                         broadcast_c(c_of(scn, load_v(nst, taun, rowA), pkr), ccA);
                         if constexpr (READOUT) {
-                            const float pqr = reduce_slots<NCL, RG>(pAq, lane);
+                            const float pqr = reduce_group(pAq);
                             if (o_lane) store_o(o_t, rowA, sct.x * pqr);
                         }
                     }
@@ -828,7 +841,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     // group B's readout of the last token
     if constexpr (READOUT) {
         if (ok && len > 0) {
-            const float pqr = reduce_slots<NCL, RG>(pBq, lane);
+            const float pqr = reduce_group(pBq);
             if (o_lane && !TWIN) store_o(o_head + (size_t)(len - 1) * (size_t)H * (size_t)dv, rowB, scp.x * pqr);
         }
     }
