@@ -302,7 +302,7 @@ gdn_status run_jobs(const LaunchSpec& L, std::vector<HostJob>& jobs, cudaStream_
     const int H = p->num_heads, dv = p->d_v, dk = p->d_k;
     const bool in_bf16 = p->qkv_dtype == GDN_BF16;
     const bool out_bf16 = p->out_dtype == GDN_BF16;
-    const int wr = gdn::kSlotsPerWarp / (L.twin ? 2 : 1);   // real rows per consumer warp
+    const int wr = gdn::slots_per_warp(dk) / (L.twin ? 2 : 1);   // real rows per consumer warp
     const int nw = std::min(gdn::kMaxConsumerWarps, dv / wr);
     const int rows = nw * wr;
     const int ctas_per_head = dv / rows;

@@ -10,12 +10,13 @@
 // Design (one CTA = one (job, head, block of state rows)):
 //  * Row i of S evolves only from v_{t,i}: the key-space operator acts from the
 //    right, so the rows of a head split across lanes, warps and CTAs with no
-//    exchange.  A consumer warp owns 16 state rows ("slots"): lanes form 4 row
-//    groups of 8 column lanes, and a lane holds a 4-row x (d_k/8)-column register
-//    tile, whose rows form two groups of 2 run half a token apart.  The dot products
-//    S k and S q of a group reduce over the 8 column lanes with a reduce-scatter
-//    that leaves lanes 4s..4s+3 of a row group with slot s's sums.  Two consumer
-//    warps share each SM sub-partition, hiding each other's per-token chain.
+//    exchange.  Lanes form 4 row groups of 8 column lanes; a lane holds a register
+//    tile of (d_k/8) columns and 4 rows at d_k = 128 (two groups of 2 run half a
+//    token apart; a warp owns 16 state rows, "slots"), 2 rows (one group; 8 rows
+//    a warp) below.  The dot products S k and S q of a group reduce over the 8
+//    column lanes with a reduce-scatter that leaves lanes 4s..4s+3 of a row group
+//    with slot s's sums.  Two consumer warps share each SM sub-partition (at
+//    d_k = 128, and at 64 with d_v = 64), hiding each other's per-token chain.
 //  * The state is kept in a running scale: S = s * St.  With s_t = alpha_t s_{t-1}
 //    the update becomes St += c k^T with c = (beta/s_t) v - beta (St_{t-1} k), so
 //    each state element costs exactly three FMAs per token (update, S k, S q),
@@ -48,15 +49,17 @@ constexpr int kChunk = 32;     // tokens per pipeline stage
 constexpr int kStages = 3;     // depth of the shared-memory ring
 constexpr int kMaxJobs = 256;  // jobs per launch (host splits larger batches)
 constexpr int kMaxCkpts = 1536;
-// A lane holds kRowSlots state rows x (d_k / kColLanes) columns; the rows split into two groups that run half
-// a token apart (see the consumer loop).  Shared memory serves a warp's broadcast 16-byte load in 2 cycles (64
-// floats a cycle to an SM, against 128 FMAs) and every float of k or q a lane loads feeds one FMA per row it
-// holds, so 4 rows keep the loads under the FMA time, and the 64 registers of a d_k = 128 tile leave room for
-// 8 consumer warps (two per SM sub-partition) at 168 registers.
+// A lane holds row_slots(d_k) state rows x (d_k / kColLanes) columns.  At d_k = 128 the 4 rows split into two
+// groups that run half a token apart (see the consumer loop): shared memory serves a warp's broadcast 16-byte
+// load in 2 cycles (64 floats a cycle to an SM, against 128 FMAs) and every float of k or q a lane loads feeds
+// one FMA per row it holds, so 4 rows keep the loads under the FMA time (measured: 2 rows and 16 warps, +24 %).
+// Below d_k = 128 a token's chain of dependent steps, not the loads, bounds the loop, and 2 rows a lane give
+// twice the warps for a head (measured at d_k = 32: -8 %).
 constexpr int kColLanes = 8;
-constexpr int kRowSlots = 4;
+__host__ __device__ constexpr int row_slots(int dk) { return dk == 128 ? 4 : 2; }
 constexpr int kMaxConsumerWarps = 8;
-constexpr int kSlotsPerWarp = (32 / kColLanes) * kRowSlots;   // state rows (slots) held by one consumer warp
+// state rows (slots) held by one consumer warp
+__host__ __device__ constexpr int slots_per_warp(int dk) { return (32 / kColLanes) * row_slots(dk); }
 // With d_k = 128 the warps stage their own inputs (see the kernel): 8 warps of 64-register tiles then may use
 // 255 registers, where a producer warp as a ninth would cap them at 168 (measured: -20 % time).  The smaller
 // sizes keep a producer warp (at most 4 + 1 warps, already under no cap), which spares them the staging work.
@@ -281,8 +284,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     gdn_scan_kernel(const __grid_constant__ Params p) {
     constexpr int ES = IN_BF16 ? 2 : 4;
     constexpr int NCL = kColLanes;           // column lanes per row group
-    constexpr int RT = kRowSlots;            // row slots per lane
-    constexpr int RG = RT / 2;               // slots of one of the lane's two row groups (A: 0..RG-1, B: RG..)
+    constexpr int RT = row_slots(DK);        // row slots per lane
+    constexpr int RG = 2;                    // slots of a row group (reduced together)
+    constexpr int NG = RT / RG;              // row groups per lane: A (slots 0, 1) and, with 4 slots, B (2, 3)
     constexpr int LPG = NCL / RG;            // lanes that end up holding one slot's sums in a group reduction
     constexpr int CT = DK / NCL;             // columns per lane (16, 8, 4)
     constexpr int CT2 = CT / 2;
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     constexpr int HALF = TWIN ? RT / 2 : RT; // real rows per lane per state
     constexpr int WR = NRG * HALF;           // real rows per warp (16, or 8 with the twin)
     static_assert(CH4 >= 1 && CT % 4 == 0, "lane tile");
-    static_assert(NRG * RT == kSlotsPerWarp, "slots per warp");
+    static_assert(NRG * RT == slots_per_warp(DK) && (NG == 1 || NG == 2), "slots per warp");
     using OutT = typename std::conditional<OUT_BF16, __nv_bfloat16, float>::type;
     constexpr bool FOLD = staging_in_warps(DK);   // the warps stage their inputs themselves (no producer warp)
 
@@ -441,10 +445,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     }
 
     // ================================ consumer warps ===============================
-    // The lane's RT slots form two row groups, A (slots 0..RG-1) and B (RG..RT-1), run half a token apart:
+    // With 4 slots the lane's rows form two row groups, A (slots 0, 1) and B (2, 3), run half a token apart:
     // group B's reduction, c and readout of one token are issued between group A's FMAs of the next, and
     // group A's between group B's, so that neither group waits for its own shuffles.  With the twin, A is
-    // the scan and B the twin.
+    // the scan and B the twin.  With 2 slots there is only group A (with the twin: slot 0 the scan's row,
+    // slot 1 the twin's).
     const int cl = lane & (NCL - 1);
     const int rg = lane / NCL;
     const int row0 = warp * WR + rg * HALF;                              // CTA row of this group's slot 0
@@ -452,7 +457,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     // With swapped_rows(DK) the lanes whose sums end up in slot 1 of a group hold the group's two rows in
     // swapped registers, so that every lane's first reduction round keeps register 0 and sends register 1:
     // register i of group g then holds slot g * RG + (i ^ gslot) (else slot i).
-    static_assert(RG == 2 && LPG == NCL / 2 && (!TWIN || HALF == RG),
+    static_assert(LPG == NCL / 2 && (!TWIN || NG == 1 || HALF == RG),
                   "two slots per group, reduced over the column lanes; the twin form's groups are its two states");
     constexpr bool SWAP = swapped_rows(DK);
     const int rswap = SWAP ? gslot : 0;
@@ -461,7 +466,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
         else return i;
     };
     auto reduce_group = [&](float (&v)[RG]) { return reduce_pair<NCL, SWAP>(v, lane); };
-    const int rowA = row0 + gslot;                                       // CTA-relative real rows of those slots
+    // CTA-relative real rows of those slots (one group with the twin: slot 0 the scan's row, slot 1 the twin's)
+    const int rowA = row0 + ((TWIN && NG == 1) ? 0 : gslot);
     const int rowB = row0 + (TWIN ? gslot : RG + gslot);
     const int grow_base = rb * RB + row0;                                // head row of slot 0
     const size_t head_state = (size_t)h * (size_t)dv * DK;
@@ -470,8 +476,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     float2 S[RT][CT2];
 #pragma unroll
     for (int i = 0; i < RT; ++i) {
-        const int state = TWIN ? i / RG : 0;                             // the twin form's group g is state g
-        const int grow = grow_base + (TWIN ? slot_of(i) % RG : slot_of(i));
+        // with the twin, group g (two groups) or slot g (one group) is state g
+        const int state = TWIN ? (NG == 2 ? i / RG : slot_of(i)) : 0;
+        const int grow = grow_base + (TWIN ? slot_of(i) % HALF : slot_of(i));
         const float* src = state == 0 ? p.jobs[job_idx].s0 : p.jobs[job_idx].s0_twin;
 #pragma unroll
         for (int j4 = 0; j4 < CH4; ++j4) {
@@ -565,8 +572,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
     auto store_state = [&](float* dst_head, int which) {
 #pragma unroll
         for (int i = 0; i < RT; ++i) {
-            if ((TWIN ? i / RG : 0) != which) continue;
-            const int grow = grow_base + (TWIN ? slot_of(i) % RG : slot_of(i));
+            if ((TWIN ? (NG == 2 ? i / RG : slot_of(i)) : 0) != which) continue;
+            const int grow = grow_base + (TWIN ? slot_of(i) % HALF : slot_of(i));
 #pragma unroll
             for (int j4 = 0; j4 < CH4; ++j4) {
                 const float2 a0 = S[i][2 * j4 + 0], a1 = S[i][2 * j4 + 1];
@@ -578,7 +585,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
 
     void* const o_job = p.jobs[job_idx].o;
     OutT* const o_head = reinterpret_cast<OutT*>(o_job) + (size_t)h * (size_t)dv + (size_t)(rb * RB);
-    const bool o_lane = READOUT && o_job != nullptr && (cl % LPG) == 0;
+    const bool o_lane = READOUT && o_job != nullptr && (cl % LPG) == 0 && (NG == 2 || !TWIN || gslot == 0);
     auto store_o = [&](OutT* o_tok, int row, float val) {
         OutT* op = o_tok + row;
         if constexpr (OUT_BF16)
@@ -596,7 +603,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
         dot_group(0, ktok, pk);
         const float pkr = reduce_group(pk);
         broadcast_c(c_of(sc, load_v(stg, tau, rowA), pkr), ccA);
-        dot_group(1, ktok, pBk);
+        if constexpr (NG == 2) dot_group(1, ktok, pBk);
     };
 
     // ---- (d_k = 128) input staging by the warps themselves (no producer warp: a ninth warp would cap every
@@ -778,7 +785,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
                     load_k(k_nxt, kn);
 
                     // group B: c_t from St_{t-1} k_t, and its readout of token t-1
-                    {
+                    if constexpr (NG == 2) {
                         const float pkr = reduce_group(pBk);
                         broadcast_c(c_of(sct, load_v(stage, tau, rowB), pkr), ccB);
                         if constexpr (READOUT) {
@@ -799,7 +806,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
                         }
                     }
                     // group B: token t
-                    group_pass(1, ccB, kc, kn, q_cur, pBk, pBq);
+                    if constexpr (NG == 2) group_pass(1, ccB, kc, kn, q_cur, pBk, pBq);
 
                     const bool renorm = (__float_as_uint(sct.w) & FLAG_RENORM) != 0u;
                     scp = sct;
@@ -839,7 +846,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + (staging_in_warps(DK
         }
     }
     // group B's readout of the last token
-    if constexpr (READOUT) {
+    if constexpr (READOUT && NG == 2) {
         if (ok && len > 0) {
             const float pqr = reduce_group(pBq);
             if (o_lane && !TWIN) store_o(o_head + (size_t)(len - 1) * (size_t)H * (size_t)dv, rowB, scp.x * pqr);
