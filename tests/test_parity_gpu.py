@@ -360,14 +360,16 @@ def test_row_permutation_equivariance(algo):
     assert torch.equal(b["o"], a["o"][:, :, pd]), "outputs: components permuted"
 
 
-@pytest.mark.parametrize("algo", ["per_token", "chunked", "chunked_mma", "two_pass"])
-def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic(algo):
+@pytest.mark.parametrize("algo,dk", [("per_token", 128), ("per_token", 64), ("per_token", 32), ("chunked", 128),
+                                     ("chunked_mma", 128), ("two_pass", 128)])
+def test_resume_is_bitwise_equal_to_full_run_and_runs_are_deterministic(algo, dk):
     """Resume from the deepest stored checkpoint c_j <= d reproduces, bit for bit,
     the state at d of a full run that stores the same checkpoints plus d.  (Each
     stored checkpoint renormalises the running scale, so the comparison run must
-    not store anything else between c_j and d.)"""
+    not store anything else between c_j and d.)  The per-token cases at d_k = 64 and 32
+    run that kernel's 2-row lane tile with its producer warp."""
     lens = [1000]
-    H, dk, dv = 3, 128, 128
+    H, dv = 3, dk
     w, inp = _inputs(51, lens, H, dk, dv, torch.bfloat16, 0.95, 1.0, beta="sigmoid")
     d = _dev(inp)
     cu = w.cu_seqlens

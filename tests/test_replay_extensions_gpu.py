@@ -117,11 +117,14 @@ def test_adaptive_plan_reads_the_gates_after_earlier_work_on_its_stream():
 
 
 def _timed(stream, fn, reps=5):
+    """Median device time of fn on stream.  The GPU is kept busy while the host enqueues fn, so that the
+    host's own time for the call (argument checks, the launch plan) is not counted."""
     fn()
     torch.cuda.synchronize()
     ts = []
     for _ in range(reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(2_000_000)
         e0.record(stream)
         fn()
         e1.record(stream)
