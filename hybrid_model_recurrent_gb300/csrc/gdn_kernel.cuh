@@ -53,8 +53,8 @@ constexpr int kMaxCkpts = 1536;
 // groups that run half a token apart (see the consumer loop): shared memory serves a warp's broadcast 16-byte
 // load in 2 cycles (64 floats a cycle to an SM, against 128 FMAs) and every float of k or q a lane loads feeds
 // one FMA per row it holds, so 4 rows keep the loads under the FMA time (measured: 2 rows and 16 warps, +24 %).
-// Below d_k = 128 a token's chain of dependent steps, not the loads, bounds the loop, and 2 rows a lane give
-// twice the warps for a head (measured at d_k = 32: -8 %).
+// Below d_k = 128 the latency of each warp's dependent shuffles and arithmetic, not the loads, bounds the loop,
+// and 2 rows a lane give twice the warps for a head (measured at d_k = 32: -8 %).
 constexpr int kColLanes = 8;
 __host__ __device__ constexpr int row_slots(int dk) { return dk == 128 ? 4 : 2; }
 constexpr int kMaxConsumerWarps = 8;
@@ -62,7 +62,8 @@ constexpr int kMaxConsumerWarps = 8;
 __host__ __device__ constexpr int slots_per_warp(int dk) { return (32 / kColLanes) * row_slots(dk); }
 // With d_k = 128 the warps stage their own inputs (see the kernel): 8 warps of 64-register tiles then may use
 // 255 registers, where a producer warp as a ninth would cap them at 168 (measured: -20 % time).  The smaller
-// sizes keep a producer warp (at most 4 + 1 warps, already under no cap), which spares them the staging work.
+// sizes keep a producer warp (at most 8 + 1 warps of under 100 registers, under no cap), which spares them the
+// staging work.
 __host__ __device__ constexpr bool staging_in_warps(int dk) { return dk == 128; }
 constexpr float kRenormFloor = 0x1p-32f;
 // Bound of the wait for this CTA's own copies in flight before it exits (independent of the
