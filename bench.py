@@ -30,6 +30,7 @@ import statistics
 import subprocess
 import sys
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -449,8 +450,9 @@ def overlap_report(dev, reps: int = 5):
             "replay_Mtok_head_per_s": k_tail * H / (t_rep * 1e-3) / 1e6}
 
 
-def workloads_report(dev, hbm_peak: float, reps: int = 5):
-    """Every synthetic workload on its own (CUDA events around `reps` back-to-back calls, per call).
+def workloads_report(dev, hbm_peak: float, reps: int = 5, only: Optional[str] = None):
+    """Every synthetic workload on its own (CUDA events around `reps` back-to-back calls, per call); with `only`,
+    that one tail-replay workload alone.
     Throughput in tok*head/s and, against the HBM peak, the algorithmic bytes of the call: per tok*head
     q, k, v + gates + o (1,032 B at bf16 d = 128) with a readout, k, v + gates (520 B) without; 64 KiB per
     state read or written.  The replay workloads are given as their tails alone (the rows the kernel reads:
@@ -483,6 +485,9 @@ def workloads_report(dev, hbm_peak: float, reps: int = 5):
         es = 2 if w.qkv_dtype == torch.bfloat16 else 4
         eo = 2 if w.out_dtype == torch.bfloat16 else 4
         return (w.dk + w.dv + (w.dk if readout else 0)) * es + 8 + (w.dv * eo if readout else 0)
+
+    if only:
+        return {only: replay_rows(gdn, dev, only, ws, timed, row, per_tok)}
 
     # tiny: prefill (readout, checkpoints every 64), 4 resume probes, tail replay r = 1/20 at m = 256 with twin
     w = synth.workload("tiny")
@@ -524,30 +529,35 @@ def workloads_report(dev, hbm_peak: float, reps: int = 5):
     del x, o, S_f, cks, o_r, S_o
     torch.cuda.empty_cache()
 
-    # tail replays: 768 scans x 1639 (5 % of 32768), with and without the exact twin; 32 ragged requests x
-    # 16 heads, k_b = ceil(m_b / 10)
+    # tail replays: replay5 and ragged10, each given as its tails alone
     for name in ("replay5", "ragged10"):
-        wf = synth.workload(name)
-        rn, rd = wf.replay_r
-        tails = [gdn.gdn_replay_plan(m, rn, rd)[1] for m in wf.seq_lens]
-        w = synth.Workload(name + "-tails", tails, wf.H, wf.dk, wf.dv, wf.qkv_dtype, wf.out_dtype, wf.alpha_lo,
-                           wf.alpha_hi, wf.beta_kind, seed=wf.seed)
-        x = synth.make_inputs(w, device=dev, with_q=False)
-        cu, D = w.cu_seqlens, w.dv * w.dk * 4
-        S_h = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
-        t = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, tails, 1, 1, S_hat=S_h, ws=ws))
-        rows = {"replay": row(t, w.T * w.H, w.T * w.H * per_tok(w, False) + w.B * w.H * D)}
-        if name == "replay5":
-            S_a = synth.state(101, w.B * w.H, w.dv, w.dk, 1.0, device=dev).view(w.B, w.H, w.dv, w.dk)
-            S_e = torch.empty_like(S_h)
-            t2 = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, tails, 1, 1, S_a=S_a,
-                                                   S_hat=S_h, S_exact=S_e, ws=ws))
-            rows["replay_with_twin"] = row(t2, 2 * w.T * w.H, w.T * w.H * per_tok(w, False) + w.B * w.H * 3 * D)
-        rows["note"] = f"{w.B * w.H} scans, {w.T * w.H} tail tok*head"
-        out[name] = rows
-        del x, S_h
-        torch.cuda.empty_cache()
+        out[name] = replay_rows(gdn, dev, name, ws, timed, row, per_tok)
     return out
+
+
+def replay_rows(gdn, dev, name, ws, timed, row, per_tok):
+    """Tail replays of one workload: replay5 (768 scans x 1639, 5 % of 32768, with and without the exact twin) or
+    ragged10 (32 ragged requests x 16 heads, k_b = ceil(m_b / 10)), given as their tails alone."""
+    wf = synth.workload(name)
+    rn, rd = wf.replay_r
+    tails = [gdn.gdn_replay_plan(m, rn, rd)[1] for m in wf.seq_lens]
+    w = synth.Workload(name + "-tails", tails, wf.H, wf.dk, wf.dv, wf.qkv_dtype, wf.out_dtype, wf.alpha_lo,
+                       wf.alpha_hi, wf.beta_kind, seed=wf.seed)
+    x = synth.make_inputs(w, device=dev, with_q=False)
+    cu, D = w.cu_seqlens, w.dv * w.dk * 4
+    S_h = torch.empty((w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    t = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, tails, 1, 1, S_hat=S_h, ws=ws))
+    rows = {"replay": row(t, w.T * w.H, w.T * w.H * per_tok(w, False) + w.B * w.H * D)}
+    if name == "replay5":
+        S_a = synth.state(101, w.B * w.H, w.dv, w.dk, 1.0, device=dev).view(w.B, w.H, w.dv, w.dk)
+        S_e = torch.empty_like(S_h)
+        t2 = timed(lambda: gdn.gdn_tail_replay(None, x.k, x.v, x.alpha, x.beta, cu, tails, 1, 1, S_a=S_a,
+                                               S_hat=S_h, S_exact=S_e, ws=ws))
+        rows["replay_with_twin"] = row(t2, 2 * w.T * w.H, w.T * w.H * per_tok(w, False) + w.B * w.H * 3 * D)
+    rows["note"] = f"{w.B * w.H} scans, {w.T * w.H} tail tok*head"
+    del x, S_h
+    torch.cuda.empty_cache()
+    return rows
 
 
 def cpu_baseline(w: synth.Workload):
@@ -801,7 +811,15 @@ def main():
     ap.add_argument("--step-only", action="store_true",
                     help="time the step (and its three-call form) only: no placement, overlap, chunked-variant or "
                          "other-workload reports (a few GB on the device, for profiler captures)")
+    ap.add_argument("--only-workload", choices=["replay5", "ragged10"],
+                    help="time that tail-replay workload alone and print its figures (for profiler captures)")
     args = ap.parse_args()
+    if args.only_workload:
+        import hybrid_model_recurrent_gb300 as gdn
+        dev = torch.device("cuda", 0)
+        gdn.build()
+        print(json.dumps(workloads_report(dev, measured_peaks()[0], only=args.only_workload)), flush=True)
+        return
     ws, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, ws, rank)
